@@ -1,0 +1,195 @@
+/*
+ * ipttt.h -- C ABI of the In-Place TTT fast-weight SwiGLU layer for NVIDIA B300 (sm_103a).
+ *
+ * The layer (zhichai.net "In-Place TTT：给LLM装上"临时记忆插槽"，让它边读边学"; ordering also in
+ * the xiaoxiang.io summary "原位测试时训练", 核心方法 item 3) computes, for each sequence b:
+ *
+ *   (1) Z      = SiLU(H W_gate^T) * (H W_up^T)                    §3.1 gated-MLP equation
+ *   (2) V      = CausalConv1D(X0) W_target                         §3.3 LM-aligned target
+ *   (3) D_i    = V_i^T Z_i for every C-token chunk i               §3.2 Step 1, §3.3 update rule
+ *   (4) W_i    = W_down0 + eta * sum_{j<i} D_j  (exclusive prefix) §3.2 Step 2, bullets 2-4
+ *   (5) O_i    = Z_i W_i^T                                          §3.1, §3.2 Step 3
+ *   and returns O and the final state W_down0 + eta * sum_j D_j.
+ *
+ * Readings fixed by this ABI (the pages are silent or garbled there):
+ *   - the conv is depthwise, zero left-padded by k-1 per sequence, no bias; conv_w[c, k-1]
+ *     multiplies the current token, conv_w[c, 0] the token k-1 steps back;
+ *   - V = Y W_target with W_target stored [d_in, d_out] (right-multiplied, as printed);
+ *   - the loss printed as -<V, Z W_down>_F is read as -<V, Z W_down^T>_F, whose negative
+ *     gradient is the printed update direction V^T Z;
+ *   - eta is applied as given; a last chunk shorter than C is a chunk of its own;
+ *   - a batch holds independent sequences, each with its own padding and its own state.
+ *
+ * Conventions for every entry point
+ *   - All tensors are dense row-major.  Device pointers are allocated and owned by the
+ *     caller; the library never allocates device memory in a compute call.  Every pointer
+ *     passed to a compute call must be 16-byte aligned.  Inputs are read only; outputs
+ *     and the workspace must not overlap the inputs or each other.
+ *   - dtype IPTTT_BF16: H, X0, weights, O, workspace tensors are bf16; products accumulate
+ *     in fp32 on the tensor cores; the running state is fp32; Z, V and the per-chunk
+ *     weights W_i are rounded to bf16 (round-to-nearest-even).  Requires C % 128 == 0.
+ *     dtype IPTTT_F32: everything fp32 on CUDA cores (any C >= 1).
+ *     Both require d % 8 == 0, d_ff % 8 == 0, 1 <= k <= 8, B*T < 2^31.
+ *   - Compute calls are asynchronous on the context's stream.  Argument errors are
+ *     reported before anything is launched.  A device-side wait that runs past the
+ *     context's limit makes the kernel record IPTTT_ERR_TIMEOUT and return; the code is
+ *     reported by the next ipttt_sync().  No call throws or aborts the process.
+ *   - Every failing call stores a message retrievable with ipttt_last_error().
+ */
+#ifndef IPTTT_H
+#define IPTTT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ipttt_ctx ipttt_ctx; /* opaque */
+
+typedef enum {
+  IPTTT_OK = 0,
+  IPTTT_ERR_INVALID_ARG = 1, /* null / misaligned / overlapping pointer, negative size ... */
+  IPTTT_ERR_UNSUPPORTED = 2, /* valid but unsupported shape or dtype combination          */
+  IPTTT_ERR_WORKSPACE = 3,   /* workspace missing or smaller than ipttt_workspace_size() */
+  IPTTT_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed                      */
+  IPTTT_ERR_TIMEOUT = 5      /* a device-side wait ran past the limit (see ipttt_sync)  */
+} ipttt_status;
+
+typedef enum { IPTTT_F32 = 0, IPTTT_BF16 = 1 } ipttt_dtype;
+
+/* Kernel stages, in launch order, as reported by ipttt_timing_read(). */
+typedef enum {
+  IPTTT_STAGE_SWIGLU = 0, /* step (1)                                     */
+  IPTTT_STAGE_CONV = 1,   /* causal conv of step (2)                      */
+  IPTTT_STAGE_TARGET = 2, /* W_target projection of step (2), times eta   */
+  IPTTT_STAGE_STATE = 3,  /* steps (3)+(4): chunk updates and prefix      */
+  IPTTT_STAGE_APPLY = 4,  /* step (5)                                     */
+  IPTTT_NUM_STAGES = 5
+} ipttt_stage;
+
+/* Library version as "major.minor.patch"; static string. */
+const char* ipttt_version(void);
+
+/* Human-readable name of a status code; static string. */
+const char* ipttt_status_string(ipttt_status s);
+
+/* Create a context on CUDA device `device`, bound to `cuda_stream` (a cudaStream_t; NULL =
+ * the legacy default stream).  Allocates a 8-byte device status word and CUDA events; this
+ * is the only call that allocates device memory.  *out receives the context.
+ * Errors: INVALID_ARG (out == NULL, bad device), CUDA. */
+ipttt_status ipttt_create(ipttt_ctx** out, int device, void* cuda_stream);
+
+/* Rebind the context to another stream of the same device. */
+ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* cuda_stream);
+
+/* Limit, in nanoseconds, on every device-side wait of later launches (default 2e9). */
+ipttt_status ipttt_set_wait_limit_ns(ipttt_ctx* ctx, uint64_t ns);
+
+/* Wait for the context's stream, then read and clear the device status word.
+ * Returns IPTTT_ERR_TIMEOUT if a kernel gave up a wait since the last sync, CUDA on a
+ * CUDA error, else OK. */
+ipttt_status ipttt_sync(ipttt_ctx* ctx);
+
+/* Message of the last failing call on this context (empty string if none). */
+const char* ipttt_last_error(const ipttt_ctx* ctx);
+
+/* Destroy a context (NULL is ignored).  Waits for nothing: sync first. */
+void ipttt_destroy(ipttt_ctx* ctx);
+
+/* Bytes of device workspace ipttt_layer_forward needs for this shape (host-only call, no
+ * GPU needed).  Layout: Y [B,T,d], V [B,T,d], Z [B,T,d_ff], W stack [B,ceil(T/C),d,d_ff],
+ * each in `dtype`, each region 256-byte aligned.
+ * Errors: INVALID_ARG (bytes == NULL, negative sizes, C < 1, k < 1), UNSUPPORTED. */
+ipttt_status ipttt_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
+                                  ipttt_dtype dtype, size_t* bytes);
+
+/* The whole layer, steps (1)-(5).
+ *   H, X0     [B, T, d]        dtype, device      hidden state; embedding output
+ *   W_gate    [d_ff, d]        dtype, device      frozen, shared by all sequences
+ *   W_up      [d_ff, d]        dtype, device      frozen
+ *   W_down0   [d, d_ff]        dtype, device      initial fast weight
+ *   W_target  [d, d]           dtype, device      [d_in, d_out], V = Y W_target
+ *   conv_w    [d, k]           dtype, device      depthwise causal taps
+ *   O         [B, T, d]        dtype, device      output
+ *   W_final   [B, d, d_ff]     fp32,  device      state after the last chunk's update
+ *   workspace                  device, >= ipttt_workspace_size() bytes, overwritten
+ * B = 0 is a no-op; T = 0 sets W_final[b] = W_down0 for every b.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA (launch). */
+ipttt_status ipttt_layer_forward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                 const void* W_up, const void* W_down0, const void* W_target,
+                                 const void* conv_w, int64_t B, int64_t T, int64_t d, int64_t d_ff,
+                                 int64_t C, int k, float eta, ipttt_dtype dtype, void* O,
+                                 float* W_final, void* workspace, size_t workspace_bytes);
+
+/* Bytes of device workspace ipttt_layer_forward_host needs: ipttt_workspace_size() plus
+ * device staging for H, X0, O and W_final. */
+ipttt_status ipttt_host_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
+                                       ipttt_dtype dtype, size_t* bytes);
+
+/* The whole layer with the activations and results in HOST memory (pinned memory gives
+ * asynchronous copies): H_host, X0_host [B,T,d] dtype are copied to the device, the layer
+ * runs, O_host [B,T,d] dtype and W_final_host [B,d,d_ff] fp32 are copied back, all in order
+ * on the context's stream.  The frozen weights stay device pointers.  The host buffers
+ * must stay valid until ipttt_sync() returns.  Errors as ipttt_layer_forward. */
+ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const void* X0_host,
+                                      const void* W_gate, const void* W_up, const void* W_down0,
+                                      const void* W_target, const void* conv_w, int64_t B, int64_t T,
+                                      int64_t d, int64_t d_ff, int64_t C, int k, float eta,
+                                      ipttt_dtype dtype, void* O_host, float* W_final_host,
+                                      void* workspace, size_t workspace_bytes);
+
+/* ---- the individual steps (the layer is exactly these calls in this order) ---- */
+
+/* Step (1), §3.1: Z[r] = SiLU(H[r] W_gate^T) * (H[r] W_up^T) for rows r < rows (rows = B*T).
+ * H [rows, d], W_gate/W_up [d_ff, d], Z [rows, d_ff], all dtype. */
+ipttt_status ipttt_swiglu(ipttt_ctx* ctx, const void* H, const void* W_gate, const void* W_up,
+                          int64_t rows, int64_t d, int64_t d_ff, ipttt_dtype dtype, void* Z);
+
+/* Step (2), §3.3: Y = CausalConv1D(X0) (per sequence), V = scale * (Y W_target).
+ * X0 [B,T,d], conv_w [d,k], W_target [d,d], Y (scratch, written) [B,T,d], V [B,T,d]. */
+ipttt_status ipttt_target(ipttt_ctx* ctx, const void* X0, const void* conv_w, const void* W_target,
+                          int64_t B, int64_t T, int64_t d, int k, float scale, ipttt_dtype dtype,
+                          void* Y, void* V);
+
+/* Steps (3)+(4), §3.2 Steps 1-2, §3.3 update: with V already scaled by eta,
+ * W_eff[b, i] = W_down0 + sum_{j<i} V_j^T Z_j and W_final[b] = W_down0 + sum_j V_j^T Z_j.
+ * V [B,T,d], Z [B,T,d_ff], W_down0 [d,d_ff] dtype; W_eff [B,ceil(T/C),d,d_ff] dtype;
+ * W_final [B,d,d_ff] fp32.  Requires T >= 1. */
+ipttt_status ipttt_chunk_state(ipttt_ctx* ctx, const void* V, const void* Z, const void* W_down0,
+                               int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C,
+                               ipttt_dtype dtype, void* W_eff, float* W_final);
+
+/* Step (5), §3.2 Step 3: O[b, chunk i] = Z[b, chunk i] W_eff[b, i]^T.
+ * Z [B,T,d_ff], W_eff [B,ceil(T/C),d,d_ff], O [B,T,d], all dtype.  Requires T >= 1. */
+ipttt_status ipttt_chunk_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t B, int64_t T,
+                               int64_t d, int64_t d_ff, int64_t C, ipttt_dtype dtype, void* O);
+
+/* ---- measurement and self-test ---- */
+
+/* Start timing: later layer calls record a CUDA event at every stage boundary (up to 256
+ * calls); earlier records are discarded. */
+ipttt_status ipttt_timing_begin(ipttt_ctx* ctx);
+
+/* Stop timing and read it: waits for the recorded events, then writes the summed device
+ * time in ms of each stage to ms[IPTTT_NUM_STAGES], the number of timed layer calls to
+ * *calls and the number of kernels those calls launched to *launches. */
+ipttt_status ipttt_timing_read(ipttt_ctx* ctx, double* ms, int64_t* calls, int64_t* launches);
+
+/* Number of kernels one ipttt_layer_forward call launches for this shape (host only). */
+int64_t ipttt_layer_launches(int64_t B, int64_t T, ipttt_dtype dtype);
+
+/* Launch one block that waits on a shared-memory barrier nothing ever signals, through
+ * the same bounded wait as the layer's kernels; it returns after the context's wait limit.
+ * The following ipttt_sync() must return IPTTT_ERR_TIMEOUT and the context stays usable. */
+ipttt_status ipttt_selftest_wait_timeout(ipttt_ctx* ctx);
+
+/* Number of streaming multiprocessors of the context's device. */
+int ipttt_sm_count(const ipttt_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IPTTT_H */

@@ -1,0 +1,95 @@
+"""Host-only checks of the C ABI (no GPU needed): the library builds, loads and exports
+every entry point include/ipttt.h declares, and the host-side validation answers."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_mlp_layers_swiglu_b300 as pkg
+from weight_mlp_layers_swiglu_b300 import native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ipttt.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ipttt_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_surface():
+    names = declared_functions()
+    assert "ipttt_layer_forward" in names and "ipttt_create" in names
+    assert sorted(native.exported_symbols()) == names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = pkg.load()
+    out = os.popen(f"nm -D --defined-only {native._build.LIB_PATH}").read()
+    exported = set(re.findall(r" T (ipttt_[a-z_]+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_version_and_status_strings():
+    lib = pkg.load()
+    assert re.match(rb"^\d+\.\d+\.\d+$", lib.ipttt_version())
+    assert lib.ipttt_status_string(0) == b"IPTTT_OK"
+    assert lib.ipttt_status_string(5) == b"IPTTT_ERR_TIMEOUT"
+
+
+def _ws(*args):
+    lib = pkg.load()
+    out = ctypes.c_size_t(0)
+    st = lib.ipttt_workspace_size(*args, ctypes.byref(out))
+    return st, out.value
+
+
+def test_workspace_size_layout():
+    B, T, d, f, C, k = 2, 1000, 256, 512, 128, 4
+    st, n = _ws(B, T, d, f, C, k, pkg.BF16)
+    assert st == 0
+    a = lambda x: (x + 255) // 256 * 256
+    nch = (T + C - 1) // C
+    assert n == a(B * T * d * 2) * 2 + a(B * T * f * 2) + a(B * nch * d * f * 2)
+    st, n32 = _ws(B, T, d, f, C, k, pkg.F32)
+    assert st == 0 and n32 == a(B * T * d * 4) * 2 + a(B * T * f * 4) + a(B * nch * d * f * 4)
+    # the 4B-shaped 32k workload fits comfortably in HBM
+    st, n = _ws(1, 32768, 2560, 9728, 1024, 4, pkg.BF16)
+    assert st == 0 and n < 3e9
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 64, 256, 512, 100, 4, 1), 2),    # bf16 needs C % 128 == 0
+    ((1, 64, 256, 512, 100, 4, 0), 0),    # fp32 takes any C
+    ((1, 64, 250, 512, 128, 4, 1), 2),    # d % 8
+    ((1, 64, 256, 500, 128, 4, 1), 2),    # d_ff % 8
+    ((1, 64, 256, 512, 128, 9, 1), 2),    # k > 8
+    ((1, 64, 256, 512, 128, 0, 1), 1),    # k < 1
+    ((-1, 64, 256, 512, 128, 4, 1), 1),   # negative B
+    ((1, -5, 256, 512, 128, 4, 1), 1),    # negative T
+    ((1, 64, 256, 512, 0, 4, 1), 1),      # C < 1
+    ((1, 64, 256, 512, 128, 4, 7), 1),    # unknown dtype
+    ((0, 0, 256, 512, 128, 4, 1), 0),     # empty batch is fine
+])
+def test_workspace_size_validation(args, code):
+    st, _ = _ws(*args)
+    assert st == code
+
+
+def test_null_context_and_outputs_are_rejected():
+    lib = pkg.load()
+    assert lib.ipttt_workspace_size(1, 1, 8, 8, 1, 1, 0, None) == 1
+    assert lib.ipttt_sync(None) == 1
+    assert lib.ipttt_layer_forward(None, *([None] * 7), 1, 1, 8, 8, 1, 1, 0.1, 0, None, None, None, 0) == 1
+    lib.ipttt_destroy(None)
+
+
+def test_launch_counts():
+    assert pkg.layer_launches(1, 32768, pkg.BF16) == 5
+    assert pkg.layer_launches(1, 2048, pkg.F32) == 6
+    assert pkg.layer_launches(3, 0, pkg.BF16) == 1
+    assert pkg.layer_launches(0, 100, pkg.BF16) == 0

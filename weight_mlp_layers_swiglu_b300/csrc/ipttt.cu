@@ -1,0 +1,853 @@
+// Host orchestration and C ABI of the In-Place TTT fast-weight SwiGLU layer (see
+// include/ipttt.h for the contract).  bf16 runs on the tcgen05 kernels (tc_gemm.cuh,
+// tc_state.cuh); fp32 runs on the CUDA-core kernels (simt.cuh).  Nothing here computes on
+// the host: every step of the layer is a kernel launch on the context's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/ipttt.h"
+#include "ptx.cuh"
+#include "simt.cuh"
+#include "tc_gemm.cuh"
+#include "tc_state.cuh"
+
+using namespace ipttt;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+namespace {
+
+constexpr int kMaxTimedCalls = 256;
+constexpr int kBoundaries = IPTTT_NUM_STAGES + 1;
+
+}  // namespace
+
+struct ipttt_ctx {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  int sm_count = 0;
+  uint32_t* status = nullptr;  // device, 2 words
+  uint64_t wait_limit_ns = 2000000000ull;
+  EncodeTiledFn encode = nullptr;
+  bool attrs_set = false;
+  // timing
+  bool timing = false;
+  int timed_calls = 0;
+  int64_t timed_launches = 0;
+  std::vector<cudaEvent_t> events;
+  std::string err;
+};
+
+namespace {
+
+void set_err(ipttt_ctx* ctx, const char* fmt, ...) {
+  if (!ctx) return;
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  ctx->err = buf;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+size_t esize(ipttt_dtype dt) { return dt == IPTTT_BF16 ? 2 : 4; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Region {
+  const void* p;
+  size_t bytes;
+  const char* name;
+};
+
+// Finds the first pair (output region, any other region) whose byte ranges intersect.
+bool find_overlap(const std::vector<Region>& outs, const std::vector<Region>& all, std::string& what) {
+  for (const Region& o : outs) {
+    if (!o.p || o.bytes == 0) continue;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(o.p), a1 = a0 + o.bytes;
+    for (const Region& r : all) {
+      if (!r.p || r.bytes == 0 || std::strcmp(r.name, o.name) == 0) continue;
+      const uintptr_t b0 = reinterpret_cast<uintptr_t>(r.p), b1 = b0 + r.bytes;
+      if (a0 < b1 && b0 < a1) {
+        what = std::string(o.name) + " / " + r.name;
+        return true;
+      }
+    }
+  }
+  return false;
+}
+
+// Shape rules shared by every entry point.  ctx may be null (host-only callers).
+ipttt_status check_shape(ipttt_ctx* ctx, int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, int k,
+                         ipttt_dtype dt, bool need_C = true) {
+  if (dt != IPTTT_F32 && dt != IPTTT_BF16) {
+    set_err(ctx, "unknown dtype %d", (int)dt);
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (B < 0 || T < 0 || d < 1 || f < 1 || k < 1 || (need_C && C < 1)) {
+    set_err(ctx, "invalid sizes B=%lld T=%lld d=%lld d_ff=%lld C=%lld k=%d", (long long)B, (long long)T,
+            (long long)d, (long long)f, (long long)C, k);
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (d % 8 || f % 8) {
+    set_err(ctx, "d (%lld) and d_ff (%lld) must be multiples of 8", (long long)d, (long long)f);
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  if (k > simt::CONV_MAXK) {
+    set_err(ctx, "conv kernel size k=%d > %d", k, simt::CONV_MAXK);
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  if (dt == IPTTT_BF16 && need_C && C % 128) {
+    set_err(ctx, "bf16 path needs C %% 128 == 0 (C=%lld)", (long long)C);
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (B * T > lim || d > (1 << 20) || f > (1 << 22) || (need_C && C > lim)) {
+    set_err(ctx, "sizes exceed the supported range");
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  return IPTTT_OK;
+}
+
+int64_t n_chunks_of(int64_t T, int64_t C) { return T == 0 ? 0 : (T + C - 1) / C; }
+
+struct WsLayout {
+  size_t y, v, z, w, total;
+};
+
+WsLayout ws_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, ipttt_dtype dt) {
+  const size_t es = esize(dt);
+  WsLayout L;
+  size_t off = 0;
+  L.y = off;
+  off += align256((size_t)B * T * d * es);
+  L.v = off;
+  off += align256((size_t)B * T * d * es);
+  L.z = off;
+  off += align256((size_t)B * T * f * es);
+  L.w = off;
+  off += align256((size_t)B * n_chunks_of(T, C) * d * f * es);
+  L.total = off;
+  return L;
+}
+
+ipttt_status cuda_fail(ipttt_ctx* ctx, cudaError_t e, const char* what) {
+  set_err(ctx, "%s: %s", what, cudaGetErrorString(e));
+  return IPTTT_ERR_CUDA;
+}
+
+ipttt_status check_launch(ipttt_ctx* ctx, const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, what);
+  return IPTTT_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+bool encode_map(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides_bytes, const uint32_t* box) {
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bx[3], es[3];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  const CUresult r =
+      ctx->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_err(ctx, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return false;
+  }
+  return true;
+}
+
+// [rows, cols] bf16 row-major, box = 64 columns x box_rows rows.
+bool map_2d(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_cols,
+            uint32_t box_rows) {
+  const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)cols * 2};
+  const uint32_t box[2] = {box_cols, box_rows};
+  return encode_map(ctx, m, base, 2, dims, strides, box);
+}
+
+// [outer, mid, inner] bf16 row-major, box = 64 inner x box_mid x 1.
+bool map_3d(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int64_t mid, int64_t inner,
+            uint32_t box_mid) {
+  const uint64_t dims[3] = {(uint64_t)inner, (uint64_t)mid, (uint64_t)outer};
+  const uint64_t strides[2] = {(uint64_t)inner * 2, (uint64_t)inner * mid * 2};
+  const uint32_t box[3] = {64, box_mid, 1};
+  return encode_map(ctx, m, base, 3, dims, strides, box);
+}
+
+ipttt_status ensure_attrs(ipttt_ctx* ctx) {
+  if (ctx->attrs_set) return IPTTT_OK;
+  cudaError_t e;
+  e = cudaFuncSetAttribute(gemm::tc_gemm_kernel<gemm::kSwiglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           gemm::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (swiglu)");
+  e = cudaFuncSetAttribute(gemm::tc_gemm_kernel<gemm::kTarget>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           gemm::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (target)");
+  e = cudaFuncSetAttribute(gemm::tc_gemm_kernel<gemm::kApply>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           gemm::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (apply)");
+  e = cudaFuncSetAttribute(state::tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           state::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (state)");
+  ctx->attrs_set = true;
+  return IPTTT_OK;
+}
+
+DevStatus dev_status(ipttt_ctx* ctx) { return DevStatus{ctx->status, ctx->wait_limit_ns}; }
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// ------------------------------------------------------------------ step launchers (no validation)
+
+ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const void* Wu, int64_t rows, int64_t d,
+                        int64_t f, ipttt_dtype dt, void* Z) {
+  if (rows == 0) return IPTTT_OK;
+  if (dt == IPTTT_BF16) {
+    CUtensorMap ma, mb0, mb1;
+    if (!map_2d(ctx, &ma, H, rows, d, 64, 128) || !map_2d(ctx, &mb0, Wg, f, d, 64, 128) ||
+        !map_2d(ctx, &mb1, Wu, f, d, 64, 128))
+      return IPTTT_ERR_CUDA;
+    gemm::Params p{};
+    p.m_tiles = ceil_div(rows, gemm::BM);
+    p.n_tiles = ceil_div(f, 128);
+    p.k_blocks = ceil_div(d, gemm::BK);
+    p.problems = 1;
+    p.group_m = 16;
+    p.out = static_cast<__nv_bfloat16*>(Z);
+    p.out_ld = f;
+    p.rows = (int)rows;
+    p.cols = (int)f;
+    p.scale = 1.f;
+    p.st = dev_status(ctx);
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+    gemm::tc_gemm_kernel<gemm::kSwiglu><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb0, mb1, p);
+  } else {
+    simt::SgemmParams p{};
+    p.A = static_cast<const float*>(H);
+    p.B = static_cast<const float*>(Wg);
+    p.B2 = static_cast<const float*>(Wu);
+    p.Cm = static_cast<float*>(Z);
+    p.M = (int)rows;
+    p.N = (int)f;
+    p.K = (int)d;
+    p.a_sm = d, p.a_sk = 1, p.b_sk = 1, p.b_sn = d, p.c_sm = f;
+    p.scale = 1.f;
+    dim3 grid(ceil_div(f, simt::SG_BN), ceil_div(rows, simt::SG_BM), 1);
+    simt::sgemm_kernel<true><<<grid, 256, 0, ctx->stream>>>(p);
+  }
+  return check_launch(ctx, "swiglu launch");
+}
+
+template <typename E>
+void launch_conv(ipttt_ctx* ctx, dim3 grid, dim3 block, const void* X0, const void* cw, void* Y, int T_len, int d,
+                 int k) {
+  const E* x = static_cast<const E*>(X0);
+  const E* w = static_cast<const E*>(cw);
+  E* y = static_cast<E*>(Y);
+  switch (k) {
+#define IPTTT_CONV_CASE(KK) \
+  case KK: simt::causal_conv_kernel<E, KK><<<grid, block, 0, ctx->stream>>>(x, w, y, T_len, d); break;
+    IPTTT_CONV_CASE(1) IPTTT_CONV_CASE(2) IPTTT_CONV_CASE(3) IPTTT_CONV_CASE(4)
+    IPTTT_CONV_CASE(5) IPTTT_CONV_CASE(6) IPTTT_CONV_CASE(7) IPTTT_CONV_CASE(8)
+#undef IPTTT_CONV_CASE
+    default: break;
+  }
+}
+
+ipttt_status run_conv(ipttt_ctx* ctx, const void* X0, const void* cw, int64_t B, int64_t T, int64_t d, int k,
+                      ipttt_dtype dt, void* Y) {
+  if (B == 0 || T == 0) return IPTTT_OK;
+  dim3 block(32, 4);
+  dim3 grid(ceil_div(d / 8, 32), ceil_div(T, (int64_t)simt::CONV_TS * 4), (unsigned)B);
+  if (dt == IPTTT_BF16)
+    launch_conv<__nv_bfloat16>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k);
+  else
+    launch_conv<float>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k);
+  return check_launch(ctx, "conv launch");
+}
+
+ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int64_t rows, int64_t d, float scale,
+                             ipttt_dtype dt, void* V) {
+  if (rows == 0) return IPTTT_OK;
+  if (dt == IPTTT_BF16) {
+    CUtensorMap ma, mb;
+    if (!map_2d(ctx, &ma, Y, rows, d, 64, 128) || !map_2d(ctx, &mb, Wt, d, d, 64, 64)) return IPTTT_ERR_CUDA;
+    gemm::Params p{};
+    p.m_tiles = ceil_div(rows, gemm::BM);
+    p.n_tiles = ceil_div(d, gemm::BN);
+    p.k_blocks = ceil_div(d, gemm::BK);
+    p.problems = 1;
+    p.group_m = 16;
+    p.out = static_cast<__nv_bfloat16*>(V);
+    p.out_ld = d;
+    p.rows = (int)rows;
+    p.cols = (int)d;
+    p.scale = scale;
+    p.st = dev_status(ctx);
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+    gemm::tc_gemm_kernel<gemm::kTarget><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, p);
+  } else {
+    simt::SgemmParams p{};
+    p.A = static_cast<const float*>(Y);
+    p.B = static_cast<const float*>(Wt);
+    p.Cm = static_cast<float*>(V);
+    p.M = (int)rows;
+    p.N = (int)d;
+    p.K = (int)d;
+    p.a_sm = d, p.a_sk = 1, p.b_sk = d, p.b_sn = 1, p.c_sm = d;
+    p.scale = scale;
+    dim3 grid(ceil_div(d, simt::SG_BN), ceil_div(rows, simt::SG_BM), 1);
+    simt::sgemm_kernel<false><<<grid, 256, 0, ctx->stream>>>(p);
+  }
+  return check_launch(ctx, "target launch");
+}
+
+// Steps (3)+(4).  fp32: Step 1 (all Delta_i) then Step 2 (scan); bf16: one fused kernel.
+ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
+                       int64_t d, int64_t f, int64_t C, ipttt_dtype dt, void* W_eff, float* W_final,
+                       bool split_timing = false, int call = -1) {
+  const int64_t n = n_chunks_of(T, C);
+  if (B == 0 || n == 0) return IPTTT_OK;
+  if (dt == IPTTT_BF16) {
+    CUtensorMap mv, mz;
+    if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64)) return IPTTT_ERR_CUDA;
+    state::Params p{};
+    p.B = (int)B;
+    p.T = (int)T;
+    p.d = (int)d;
+    p.f = (int)f;
+    p.C = (int)C;
+    p.n_chunks = (int)n;
+    p.m_units = ceil_div(d, state::BMD);
+    p.n_units = ceil_div(f, state::BNF);
+    p.units = (int)(B * p.m_units * p.n_units);
+    p.W0 = static_cast<const __nv_bfloat16*>(W0);
+    p.W_eff = static_cast<__nv_bfloat16*>(W_eff);
+    p.W_final = W_final;
+    p.st = dev_status(ctx);
+    const int pairs = (p.units + 1) / 2;
+    const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
+    state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, p);
+    return check_launch(ctx, "state launch");
+  }
+  (void)split_timing;
+  (void)call;
+  simt::SgemmParams p{};
+  p.A = static_cast<const float*>(V);
+  p.B = static_cast<const float*>(Z);
+  p.Cm = static_cast<float*>(W_eff);
+  p.M = (int)d;
+  p.N = (int)f;
+  p.K = (int)C;
+  p.a_sm = 1, p.a_sk = d, p.b_sk = f, p.b_sn = 1, p.c_sm = f;
+  p.a_tok = d, p.b_tok = f, p.c_tok = 0;
+  p.a_z = 0, p.b_z = 0, p.c_z = d * f;
+  p.chunked = 2;
+  p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
+  p.scale = 1.f;
+  dim3 grid(ceil_div(f, simt::SG_BN), ceil_div(d, simt::SG_BM), (unsigned)(B * n));
+  simt::sgemm_kernel<false><<<grid, 256, 0, ctx->stream>>>(p);
+  ipttt_status s = check_launch(ctx, "delta launch");
+  if (s != IPTTT_OK) return s;
+  const int64_t df = d * f;
+  dim3 g2(ceil_div(df, 256), (unsigned)B);
+  simt::chunk_scan_f32_kernel<<<g2, 256, 0, ctx->stream>>>(static_cast<float*>(W_eff), static_cast<const float*>(W0),
+                                                             W_final, (int)B, (int)n, df);
+  return check_launch(ctx, "scan launch");
+}
+
+ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t B, int64_t T, int64_t d, int64_t f,
+                       int64_t C, ipttt_dtype dt, void* O) {
+  const int64_t n = n_chunks_of(T, C);
+  if (B == 0 || n == 0) return IPTTT_OK;
+  if (dt == IPTTT_BF16) {
+    CUtensorMap ma, mb;
+    if (!map_3d(ctx, &ma, Z, B, T, f, 128) || !map_3d(ctx, &mb, W_eff, B * n, d, f, 256)) return IPTTT_ERR_CUDA;
+    gemm::Params p{};
+    p.m_tiles = (int)(C / gemm::BM);
+    p.n_tiles = ceil_div(d, gemm::BN);
+    p.k_blocks = ceil_div(f, gemm::BK);
+    p.problems = (int)(B * n);
+    p.group_m = 16;
+    p.out = static_cast<__nv_bfloat16*>(O);
+    p.out_ld = d;
+    p.rows = (int)T;
+    p.cols = (int)d;
+    p.scale = 1.f;
+    p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
+    p.st = dev_status(ctx);
+    const int tiles = p.problems * p.m_tiles * p.n_tiles;
+    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+    gemm::tc_gemm_kernel<gemm::kApply><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, p);
+  } else {
+    simt::SgemmParams p{};
+    p.A = static_cast<const float*>(Z);
+    p.B = static_cast<const float*>(W_eff);
+    p.Cm = static_cast<float*>(O);
+    p.M = (int)C;
+    p.N = (int)d;
+    p.K = (int)f;
+    p.a_sm = f, p.a_sk = 1, p.b_sk = 1, p.b_sn = f, p.c_sm = d;
+    p.a_tok = f, p.b_tok = 0, p.c_tok = d;
+    p.a_z = 0, p.b_z = d * f, p.c_z = 0;
+    p.chunked = 1;
+    p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
+    p.scale = 1.f;
+    dim3 grid(ceil_div(d, simt::SG_BN), ceil_div(C, simt::SG_BM), (unsigned)(B * n));
+    simt::sgemm_kernel<false><<<grid, 256, 0, ctx->stream>>>(p);
+  }
+  return check_launch(ctx, "apply launch");
+}
+
+void mark(ipttt_ctx* ctx, int call, int boundary) {
+  if (call >= 0) cudaEventRecord(ctx->events[(size_t)call * kBoundaries + boundary], ctx->stream);
+}
+
+// The layer on device buffers, validated by the caller.
+ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
+                       const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d, int64_t f,
+                       int64_t C, int k, float eta, ipttt_dtype dt, void* O, float* W_final, void* ws) {
+  if (B == 0) return IPTTT_OK;
+  if (T == 0) {
+    const int64_t df = d * f;
+    dim3 g(ceil_div(df, 256), (unsigned)B);
+    if (dt == IPTTT_BF16)
+      simt::broadcast_state_kernel<__nv_bfloat16><<<g, 256, 0, ctx->stream>>>(static_cast<const __nv_bfloat16*>(W0),
+                                                                              W_final, df);
+    else
+      simt::broadcast_state_kernel<float><<<g, 256, 0, ctx->stream>>>(static_cast<const float*>(W0), W_final, df);
+    return check_launch(ctx, "broadcast launch");
+  }
+  ipttt_status s = IPTTT_OK;
+  if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  const WsLayout L = ws_layout(B, T, d, f, C, dt);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* Y = base + L.y;
+  void* V = base + L.v;
+  void* Z = base + L.z;
+  void* Wst = base + L.w;
+  int call = -1;
+  if (ctx->timing && ctx->timed_calls < kMaxTimedCalls) call = ctx->timed_calls++;
+  mark(ctx, call, 0);
+  if ((s = run_swiglu(ctx, H, Wg, Wu, B * T, d, f, dt, Z)) != IPTTT_OK) return s;
+  mark(ctx, call, 1);
+  if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, Y)) != IPTTT_OK) return s;
+  mark(ctx, call, 2);
+  if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V)) != IPTTT_OK) return s;
+  mark(ctx, call, 3);
+  if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final)) != IPTTT_OK) return s;
+  mark(ctx, call, 4);
+  if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O)) != IPTTT_OK) return s;
+  mark(ctx, call, 5);
+  if (call >= 0) ctx->timed_launches += ipttt_layer_launches(B, T, dt);
+  return IPTTT_OK;
+}
+
+// Validation of the device-buffer layer call (everything except the buffers' residency).
+ipttt_status validate_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
+                            const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d,
+                            int64_t f, int64_t C, int k, float eta, ipttt_dtype dt, const void* O,
+                            const float* W_final, const void* ws, size_t ws_bytes, bool check_overlap) {
+  ipttt_status s = check_shape(ctx, B, T, d, f, C, k, dt);
+  if (s != IPTTT_OK) return s;
+  if (!std::isfinite(eta)) {
+    set_err(ctx, "eta is not finite");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (B == 0) return IPTTT_OK;
+  const size_t es = esize(dt);
+  const size_t act = (size_t)B * T * d * es;
+  struct P {
+    const void* p;
+    const char* n;
+    bool needed;
+  } ptrs[] = {{H, "H", T > 0},        {X0, "X0", T > 0},  {Wg, "W_gate", T > 0}, {Wu, "W_up", T > 0},
+              {W0, "W_down0", true},  {Wt, "W_target", T > 0}, {cw, "conv_w", T > 0}, {O, "O", T > 0},
+              {W_final, "W_final", true}, {ws, "workspace", T > 0}};
+  for (const P& q : ptrs) {
+    if (!q.needed) continue;
+    if (!q.p) {
+      set_err(ctx, "%s is NULL", q.n);
+      return IPTTT_ERR_INVALID_ARG;
+    }
+    if (!aligned16(q.p)) {
+      set_err(ctx, "%s is not 16-byte aligned", q.n);
+      return IPTTT_ERR_INVALID_ARG;
+    }
+  }
+  const WsLayout L = ws_layout(B, T, d, f, C, dt);
+  if (T > 0 && ws_bytes < L.total) {
+    set_err(ctx, "workspace too small: %zu < %zu bytes", ws_bytes, L.total);
+    return IPTTT_ERR_WORKSPACE;
+  }
+  if (check_overlap) {
+    const size_t wdf = (size_t)d * f * es;
+    std::vector<Region> all = {{H, act, "H"},
+                               {X0, act, "X0"},
+                               {Wg, wdf, "W_gate"},
+                               {Wu, wdf, "W_up"},
+                               {W0, wdf, "W_down0"},
+                               {Wt, (size_t)d * d * es, "W_target"},
+                               {cw, (size_t)d * k * es, "conv_w"},
+                               {O, act, "O"},
+                               {W_final, (size_t)B * d * f * 4, "W_final"},
+                               {ws, T > 0 ? L.total : 0, "workspace"}};
+    std::vector<Region> outs = {all[7], all[8], all[9]};
+    std::string what;
+    if (find_overlap(outs, all, what)) {
+      set_err(ctx, "overlapping buffers: %s", what.c_str());
+      return IPTTT_ERR_INVALID_ARG;
+    }
+  }
+  return IPTTT_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* ipttt_version(void) { return "0.1.0"; }
+
+const char* ipttt_status_string(ipttt_status s) {
+  switch (s) {
+    case IPTTT_OK: return "IPTTT_OK";
+    case IPTTT_ERR_INVALID_ARG: return "IPTTT_ERR_INVALID_ARG";
+    case IPTTT_ERR_UNSUPPORTED: return "IPTTT_ERR_UNSUPPORTED";
+    case IPTTT_ERR_WORKSPACE: return "IPTTT_ERR_WORKSPACE";
+    case IPTTT_ERR_CUDA: return "IPTTT_ERR_CUDA";
+    case IPTTT_ERR_TIMEOUT: return "IPTTT_ERR_TIMEOUT";
+  }
+  return "IPTTT_ERR_UNKNOWN";
+}
+
+ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
+  if (!out) return IPTTT_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  ipttt_ctx* ctx = new ipttt_ctx();
+  ctx->device = device;
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  DeviceGuard g(device);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+    delete ctx;
+    return IPTTT_ERR_CUDA;
+  }
+  ctx->sm_count = prop.multiProcessorCount;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    delete ctx;
+    return IPTTT_ERR_CUDA;
+  }
+  ctx->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  if (cudaMalloc(&ctx->status, 2 * sizeof(uint32_t)) != cudaSuccess) {
+    delete ctx;
+    return IPTTT_ERR_CUDA;
+  }
+  if (cudaMemset(ctx->status, 0, 2 * sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(ctx->status);
+    delete ctx;
+    return IPTTT_ERR_CUDA;
+  }
+  ctx->events.resize((size_t)kMaxTimedCalls * kBoundaries, nullptr);
+  for (auto& e : ctx->events) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      ipttt_destroy(ctx);
+      return IPTTT_ERR_CUDA;
+    }
+  }
+  *out = ctx;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* stream) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_set_wait_limit_ns(ipttt_ctx* ctx, uint64_t ns) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  if (ns == 0) {
+    set_err(ctx, "wait limit must be > 0");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  ctx->wait_limit_ns = ns;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_sync(ipttt_ctx* ctx) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "stream synchronize");
+  uint32_t h[2] = {0, 0};
+  e = cudaMemcpyAsync(h, ctx->status, sizeof(h), cudaMemcpyDeviceToHost, ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
+  if (h[0] != 0) {
+    const uint32_t zero[2] = {0, 0};
+    e = cudaMemcpyAsync(ctx->status, zero, sizeof(zero), cudaMemcpyHostToDevice, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "status reset");
+    set_err(ctx, "device wait gave up after %llu ns (site 0x%x)", (unsigned long long)ctx->wait_limit_ns, h[1]);
+    return h[0] == kDevStatusTimeout ? IPTTT_ERR_TIMEOUT : IPTTT_ERR_CUDA;
+  }
+  return IPTTT_OK;
+}
+
+const char* ipttt_last_error(const ipttt_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+
+void ipttt_destroy(ipttt_ctx* ctx) {
+  if (!ctx) return;
+  DeviceGuard g(ctx->device);
+  for (auto& e : ctx->events)
+    if (e) cudaEventDestroy(e);
+  if (ctx->status) cudaFree(ctx->status);
+  delete ctx;
+}
+
+ipttt_status ipttt_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k, ipttt_dtype dt,
+                                  size_t* bytes) {
+  if (!bytes) return IPTTT_ERR_INVALID_ARG;
+  const ipttt_status s = check_shape(nullptr, B, T, d, d_ff, C, k, dt);
+  if (s != IPTTT_OK) return s;
+  *bytes = ws_layout(B, T, d, d_ff, C, dt).total;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_host_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
+                                       ipttt_dtype dt, size_t* bytes) {
+  if (!bytes) return IPTTT_ERR_INVALID_ARG;
+  const ipttt_status s = check_shape(nullptr, B, T, d, d_ff, C, k, dt);
+  if (s != IPTTT_OK) return s;
+  const size_t es = esize(dt);
+  const size_t act = align256((size_t)B * T * d * es);
+  *bytes = ws_layout(B, T, d, d_ff, C, dt).total + 3 * act + align256((size_t)B * d * d_ff * 4);
+  return IPTTT_OK;
+}
+
+int64_t ipttt_layer_launches(int64_t B, int64_t T, ipttt_dtype dt) {
+  if (B <= 0) return 0;
+  if (T <= 0) return 1;
+  return dt == IPTTT_BF16 ? 5 : 6;
+}
+
+ipttt_status ipttt_layer_forward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate, const void* W_up,
+                                 const void* W_down0, const void* W_target, const void* conv_w, int64_t B, int64_t T,
+                                 int64_t d, int64_t d_ff, int64_t C, int k, float eta, ipttt_dtype dt, void* O,
+                                 float* W_final, void* ws, size_t ws_bytes) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = validate_layer(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt,
+                                  O, W_final, ws, ws_bytes, true);
+  if (s != IPTTT_OK) return s;
+  DeviceGuard g(ctx->device);
+  return run_layer(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, O, W_final, ws);
+}
+
+ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const void* X0_host, const void* W_gate,
+                                      const void* W_up, const void* W_down0, const void* W_target, const void* conv_w,
+                                      int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k, float eta,
+                                      ipttt_dtype dt, void* O_host, float* W_final_host, void* ws, size_t ws_bytes) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  size_t need = 0;
+  ipttt_status s = ipttt_host_workspace_size(B, T, d, d_ff, C, k, dt, &need);
+  if (s != IPTTT_OK) {
+    check_shape(ctx, B, T, d, d_ff, C, k, dt);
+    return s;
+  }
+  if (B == 0) return IPTTT_OK;
+  if (!ws || ws_bytes < need || !aligned16(ws)) {
+    set_err(ctx, "workspace missing, misaligned or too small: %zu < %zu bytes", ws_bytes, need);
+    return IPTTT_ERR_WORKSPACE;
+  }
+  if ((T > 0 && (!H_host || !X0_host || !O_host)) || !W_final_host) {
+    set_err(ctx, "host buffer is NULL");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  const size_t es = esize(dt);
+  const size_t act = (size_t)B * T * d * es;
+  const size_t layer_ws = ws_layout(B, T, d, d_ff, C, dt).total;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* Hd = base + layer_ws;
+  void* Xd = base + layer_ws + align256(act);
+  void* Od = base + layer_ws + 2 * align256(act);
+  float* Wfd = reinterpret_cast<float*>(base + layer_ws + 3 * align256(act));
+  s = validate_layer(ctx, T > 0 ? Hd : nullptr, T > 0 ? Xd : nullptr, W_gate, W_up, W_down0, W_target, conv_w, B, T,
+                     d, d_ff, C, k, eta, dt, T > 0 ? Od : nullptr, Wfd, ws, layer_ws, false);
+  if (s != IPTTT_OK) return s;
+  DeviceGuard g(ctx->device);
+  cudaError_t e;
+  if (T > 0) {
+    if ((e = cudaMemcpyAsync(Hd, H_host, act, cudaMemcpyHostToDevice, ctx->stream)) != cudaSuccess)
+      return cuda_fail(ctx, e, "H upload");
+    if ((e = cudaMemcpyAsync(Xd, X0_host, act, cudaMemcpyHostToDevice, ctx->stream)) != cudaSuccess)
+      return cuda_fail(ctx, e, "X0 upload");
+  }
+  s = run_layer(ctx, Hd, Xd, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, Od, Wfd, ws);
+  if (s != IPTTT_OK) return s;
+  if (T > 0 && (e = cudaMemcpyAsync(O_host, Od, act, cudaMemcpyDeviceToHost, ctx->stream)) != cudaSuccess)
+    return cuda_fail(ctx, e, "O download");
+  if ((e = cudaMemcpyAsync(W_final_host, Wfd, (size_t)B * d * d_ff * 4, cudaMemcpyDeviceToHost, ctx->stream)) !=
+      cudaSuccess)
+    return cuda_fail(ctx, e, "W_final download");
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_swiglu(ipttt_ctx* ctx, const void* H, const void* W_gate, const void* W_up, int64_t rows, int64_t d,
+                          int64_t d_ff, ipttt_dtype dt, void* Z) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, rows, 1, d, d_ff, 1, 1, dt, false);
+  if (s != IPTTT_OK) return s;
+  if (rows == 0) return IPTTT_OK;
+  if (!H || !W_gate || !W_up || !Z || !aligned16(H) || !aligned16(W_gate) || !aligned16(W_up) || !aligned16(Z)) {
+    set_err(ctx, "swiglu: NULL or misaligned pointer");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  return run_swiglu(ctx, H, W_gate, W_up, rows, d, d_ff, dt, Z);
+}
+
+ipttt_status ipttt_target(ipttt_ctx* ctx, const void* X0, const void* conv_w, const void* W_target, int64_t B,
+                          int64_t T, int64_t d, int k, float scale, ipttt_dtype dt, void* Y, void* V) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, B, T, d, 8, 1, k, dt, false);
+  if (s != IPTTT_OK) return s;
+  if (B == 0 || T == 0) return IPTTT_OK;
+  if (!X0 || !conv_w || !W_target || !Y || !V || !aligned16(X0) || !aligned16(W_target) || !aligned16(Y) ||
+      !aligned16(V)) {
+    set_err(ctx, "target: NULL or misaligned pointer");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(scale)) {
+    set_err(ctx, "scale is not finite");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  if ((s = run_conv(ctx, X0, conv_w, B, T, d, k, dt, Y)) != IPTTT_OK) return s;
+  return run_target_gemm(ctx, Y, W_target, B * T, d, scale, dt, V);
+}
+
+ipttt_status ipttt_chunk_state(ipttt_ctx* ctx, const void* V, const void* Z, const void* W_down0, int64_t B, int64_t T,
+                               int64_t d, int64_t d_ff, int64_t C, ipttt_dtype dt, void* W_eff, float* W_final) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, B, T, d, d_ff, C, 1, dt);
+  if (s != IPTTT_OK) return s;
+  if (T < 1) {
+    set_err(ctx, "chunk_state needs T >= 1");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (B == 0) return IPTTT_OK;
+  if (!V || !Z || !W_down0 || !W_eff || !W_final || !aligned16(V) || !aligned16(Z) || !aligned16(W_down0) ||
+      !aligned16(W_eff) || !aligned16(W_final)) {
+    set_err(ctx, "chunk_state: NULL or misaligned pointer");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  return run_state(ctx, V, Z, W_down0, B, T, d, d_ff, C, dt, W_eff, W_final);
+}
+
+ipttt_status ipttt_chunk_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t B, int64_t T, int64_t d,
+                               int64_t d_ff, int64_t C, ipttt_dtype dt, void* O) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, B, T, d, d_ff, C, 1, dt);
+  if (s != IPTTT_OK) return s;
+  if (T < 1) {
+    set_err(ctx, "chunk_apply needs T >= 1");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (B == 0) return IPTTT_OK;
+  if (!Z || !W_eff || !O || !aligned16(Z) || !aligned16(W_eff) || !aligned16(O)) {
+    set_err(ctx, "chunk_apply: NULL or misaligned pointer");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  return run_apply(ctx, Z, W_eff, B, T, d, d_ff, C, dt, O);
+}
+
+ipttt_status ipttt_timing_begin(ipttt_ctx* ctx) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ctx->timing = true;
+  ctx->timed_calls = 0;
+  ctx->timed_launches = 0;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_timing_read(ipttt_ctx* ctx, double* ms, int64_t* calls, int64_t* launches) {
+  if (!ctx || !ms || !calls || !launches) return IPTTT_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  ctx->timing = false;
+  for (int s = 0; s < IPTTT_NUM_STAGES; ++s) ms[s] = 0.0;
+  for (int c = 0; c < ctx->timed_calls; ++c) {
+    cudaEvent_t* ev = &ctx->events[(size_t)c * kBoundaries];
+    cudaError_t e = cudaEventSynchronize(ev[kBoundaries - 1]);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "timing event");
+    for (int s = 0; s < IPTTT_NUM_STAGES; ++s) {
+      float t = 0.f;
+      e = cudaEventElapsedTime(&t, ev[s], ev[s + 1]);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "timing elapsed");
+      ms[s] += t;
+    }
+  }
+  *calls = ctx->timed_calls;
+  *launches = ctx->timed_launches;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_selftest_wait_timeout(ipttt_ctx* ctx) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  simt::wait_probe_kernel<<<1, 32, 0, ctx->stream>>>(dev_status(ctx));
+  return check_launch(ctx, "wait probe launch");
+}
+
+int ipttt_sm_count(const ipttt_ctx* ctx) { return ctx ? ctx->sm_count : 0; }
+
+}  // extern "C"

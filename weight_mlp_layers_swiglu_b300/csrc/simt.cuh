@@ -1,0 +1,244 @@
+// CUDA-core kernels: the causal depthwise convolution (both precisions), the fp32 path of
+// the layer (generic tiled SGEMM, exclusive chunk scan), and small helpers.
+//
+// The fp32 path keeps fp32 end to end (tensor-core TF32 would not meet a 1e-4 relative
+// bound); it follows the three steps of zhichai.net "In-Place TTT：给LLM装上"临时记忆插槽"，
+// 让它边读边学" §3.2 literally: Step 1 every chunk's Delta_i = V_i^T Z_i in parallel (one
+// batched GEMM), Step 2 one exclusive prefix sum over chunks (scan kernel), Step 3 every
+// chunk applied with its own weight (one batched GEMM).
+#pragma once
+
+#include "ptx.cuh"
+
+namespace ipttt {
+namespace simt {
+
+// --------------------------------------------------------------------------- causal conv
+// Y[b, t, c] = sum_{s<k} conv_w[c, s] * X0[b, t-(k-1)+s, c], zero for t-(k-1)+s < 0
+// (zhichai.net page, §3.3: Conv1D with causal padding).  Each thread owns 8 channels and a
+// strip of CONV_TS tokens, keeping the last k-1 input rows in registers.
+constexpr int CONV_MAXK = 8;
+constexpr int CONV_TS = 32;
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const float (&v)[8]);
+template <>
+__device__ __forceinline__ void store8<float>(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 w;
+  w.x = pack_bf16x2(v[0], v[1]);
+  w.y = pack_bf16x2(v[2], v[3]);
+  w.z = pack_bf16x2(v[4], v[5]);
+  w.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = w;
+}
+
+template <typename T, int K>
+__global__ void causal_conv_kernel(const T* __restrict__ X0, const T* __restrict__ conv_w, T* __restrict__ Y,
+                                   int T_len, int d) {
+  const int cg = blockIdx.x * blockDim.x + threadIdx.x;  // channel group of 8
+  const int c0 = cg * 8;
+  const int t0 = (blockIdx.y * blockDim.y + threadIdx.y) * CONV_TS;
+  const int b = blockIdx.z;
+  if (c0 >= d || t0 >= T_len) return;
+  float w[8][K];
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+#pragma unroll
+    for (int s = 0; s < K; ++s) w[e][s] = static_cast<float>(conv_w[(int64_t)(c0 + e) * K + s]);
+  const T* xb = X0 + (int64_t)b * T_len * d + c0;
+  T* yb = Y + (int64_t)b * T_len * d + c0;
+  // win[s] holds X0[t-(K-1)+s], s < K-1, while output t is formed; win[K-1] is the current token
+  float win[K][8];
+#pragma unroll
+  for (int s = 0; s < K - 1; ++s) {
+    const int src = t0 - (K - 1) + s;
+    if (src >= 0) {
+      load8<T>(xb + (int64_t)src * d, win[s]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) win[s][e] = 0.f;
+    }
+  }
+  const int t_end = min(t0 + CONV_TS, T_len);
+  for (int t = t0; t < t_end; ++t) {
+    load8<T>(xb + (int64_t)t * d, win[K - 1]);
+    float out[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < K; ++s) acc = fmaf(w[e][s], win[s][e], acc);
+      out[e] = acc;
+    }
+    store8<T>(yb + (int64_t)t * d, out);
+#pragma unroll
+    for (int s = 0; s < K - 1; ++s)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) win[s][e] = win[s + 1][e];
+  }
+}
+
+// --------------------------------------------------------------------------- fp32 GEMM
+// C[z](m, n) = scale * sum_k A[z](m, k) * B[z](k, n), with arbitrary element strides.
+// Swiglu mode: C = SiLU(A B) * (A B2).  Chunk mode: z = b * n_chunks + i addresses chunk i of
+// sequence b; its token rows [iC, min(iC+C, T)) move the A/B/C bases by (b*T + iC) * *_tok and
+// the chunk index moves them by z * *_z; the chunk length replaces M (apply) or K (delta).
+struct SgemmParams {
+  const float* A;
+  const float* B;
+  const float* B2;
+  float* Cm;
+  int M, N, K;
+  int64_t a_sm, a_sk, b_sk, b_sn, c_sm;
+  int64_t a_tok, b_tok, c_tok;  // chunk mode: base step per token row
+  int64_t a_z, b_z, c_z;        // chunk mode: base step per chunk index
+  int chunked;                  // 0: plain; 1: chunk length is M; 2: chunk length is K
+  int T, C, n_chunks;
+  float scale;
+};
+
+constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16;
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(256) sgemm_kernel(const SgemmParams p) {
+  __shared__ float As[SG_BK][SG_BM + 4];
+  __shared__ float Bs[SG_BK][SG_BN + 4];
+  __shared__ float B2s[SWIGLU ? SG_BK : 1][SWIGLU ? SG_BN + 4 : 1];
+  const int z = blockIdx.z;
+  const float* A = p.A;
+  const float* Bm = p.B;
+  const float* B2 = p.B2;
+  float* Cm = p.Cm;
+  int M = p.M, K = p.K;
+  if (p.chunked) {
+    const int b = z / p.n_chunks;
+    const int i = z - b * p.n_chunks;
+    const int lo = i * p.C;
+    const int len = min(p.C, p.T - lo);
+    const int64_t tok = (int64_t)b * p.T + lo;
+    A += tok * p.a_tok + (int64_t)z * p.a_z;
+    Bm += tok * p.b_tok + (int64_t)z * p.b_z;
+    Cm += tok * p.c_tok + (int64_t)z * p.c_z;
+    if (p.chunked == 1) M = len; else K = len;
+  }
+  const int m0 = blockIdx.y * SG_BM;
+  const int n0 = blockIdx.x * SG_BN;
+  if (m0 >= M) return;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4] = {};
+  float acc2[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += SG_BK) {
+    for (int e = threadIdx.x; e < SG_BK * SG_BM; e += 256) {
+      const int kk = e / SG_BM, mm = e % SG_BM;
+      const int gm = m0 + mm, gk = k0 + kk;
+      As[kk][mm] = (gm < M && gk < K) ? A[gm * p.a_sm + gk * p.a_sk] : 0.f;
+    }
+    for (int e = threadIdx.x; e < SG_BK * SG_BN; e += 256) {
+      const int kk = e / SG_BN, nn = e % SG_BN;
+      const int gn = n0 + nn, gk = k0 + kk;
+      const bool in = gn < p.N && gk < K;
+      Bs[kk][nn] = in ? Bm[gk * p.b_sk + gn * p.b_sn] : 0.f;
+      if (SWIGLU) B2s[kk][nn] = in ? B2[gk * p.b_sk + gn * p.b_sn] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < SG_BK; ++kk) {
+      float a[4], bv[4], b2v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        bv[j] = Bs[kk][tx * 4 + j];
+        if (SWIGLU) b2v[j] = B2s[kk][tx * 4 + j];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
+          if (SWIGLU) acc2[i][j] = fmaf(a[i], b2v[j], acc2[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + ty * 4 + i;
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gn = n0 + tx * 4 + j;
+      if (gn >= p.N) continue;
+      float v;
+      if (SWIGLU) {
+        const float g = acc[i][j];
+        v = g / (1.0f + expf(-g)) * acc2[i][j];
+      } else {
+        v = acc[i][j] * p.scale;
+      }
+      Cm[gm * p.c_sm + gn] = v;
+    }
+  }
+}
+
+// --------------------------------------------------------------------------- exclusive scan
+// In place over the stack: on entry W[b, i] holds Delta_i (already scaled by eta); on exit
+// W[b, i] = W0 + sum_{j<i} Delta_j and W_final[b] = W0 + sum_j Delta_j.
+__global__ void chunk_scan_f32_kernel(float* __restrict__ W, const float* __restrict__ W0,
+                                      float* __restrict__ W_final, int B, int n_chunks, int64_t df) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int b = blockIdx.y;
+  if (e >= df) return;
+  float acc = W0[e];
+  float* w = W + (int64_t)b * n_chunks * df + e;
+  for (int i = 0; i < n_chunks; ++i) {
+    const float delta = w[(int64_t)i * df];
+    w[(int64_t)i * df] = acc;
+    acc += delta;
+  }
+  W_final[(int64_t)b * df + e] = acc;
+}
+
+// W_final[b] = W0 (as fp32) for every sequence: the state of an empty sequence.
+template <typename T>
+__global__ void broadcast_state_kernel(const T* __restrict__ W0, float* __restrict__ W_final, int64_t df) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < df) W_final[(int64_t)blockIdx.y * df + e] = static_cast<float>(W0[e]);
+}
+
+// Device-side wait that nothing ever signals: exercises the bounded-wait path.
+__global__ void wait_probe_kernel(DevStatus st) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bounded(&bar, 0, st, reinterpret_cast<volatile int*>(&abort_flag), 0x301);
+  __syncthreads();
+}
+
+}  // namespace simt
+}  // namespace ipttt

@@ -1,0 +1,306 @@
+// Persistent, warp-specialised bf16 GEMM on the 5th-generation tensor cores.
+//
+// One CTA per SM (192 threads):
+//   warp 0      TMA producer: streams 128x64 A tiles and 256x64 B tiles into a
+//               4-stage shared-memory ring (128-byte swizzle).
+//   warp 1      MMA issuer (one thread): tcgen05.mma 128x256x16 into one of two
+//               TMEM accumulators (2 x 256 fp32 columns), so the epilogue of one
+//               tile overlaps the main loop of the next.
+//   warps 2-5   epilogue: tcgen05.ld the accumulator (one TMEM lane = one output
+//               row per thread), apply the step's epilogue, store bf16 to HBM.
+//
+// The same kernel serves three steps of the layer (zhichai.net "In-Place TTT：给LLM装上
+// "临时记忆插槽"，让它边读边学"):
+//   Swiglu  §3.1 gated MLP:   Z = SiLU(H W_gate^T) * (H W_up^T).  The B tile holds 128
+//           rows of W_gate and the same 128 rows of W_up, so one N=256 MMA produces
+//           both halves and the epilogue fuses SiLU and the product.
+//   Target  §3.3 target:      V = scale * (Y W_target), Y = causal conv of X0 (computed
+//           by the conv kernel).  W_target is [d_in, d_out], so B is MN-major.
+//   Apply   §3.2 Step 3:      O_i = Z_i W_eff[i]^T for every chunk i of every sequence;
+//           the problem index selects the chunk's rows of Z and its slice of the
+//           W_eff stack (3-D tensor maps).
+#pragma once
+
+#include "ptx.cuh"
+
+namespace ipttt {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+
+enum Kind : int { kSwiglu = 0, kTarget = 1, kApply = 2 };
+
+struct Params {
+  int m_tiles, n_tiles, k_blocks;  // per problem
+  int problems;                    // Apply: B * n_chunks, else 1
+  int group_m;                     // rasterisation: m-tiles per group
+  __nv_bfloat16* out;
+  int64_t out_ld;  // elements between output rows
+  int rows;        // valid output rows: B*T (Swiglu, Target) or T (Apply, per sequence)
+  int cols;        // valid output columns
+  float scale;
+  int T, C, n_chunks;  // Apply only
+  DevStatus st;
+};
+
+__device__ __forceinline__ void decode_tile(const Params& p, int tile, int& prob, int& mt, int& nt) {
+  const int per_prob = p.m_tiles * p.n_tiles;
+  prob = tile / per_prob;
+  const int r = tile - prob * per_prob;
+  const int group = p.group_m * p.n_tiles;
+  const int g = r / group;
+  const int rr = r - g * group;
+  const int gm = min(p.group_m, p.m_tiles - g * p.group_m);
+  mt = g * p.group_m + rr % gm;
+  nt = rr / gm;
+}
+
+template <int KIND>
+__device__ __forceinline__ bool tile_active(const Params& p, int prob, int mt) {
+  if (KIND == kApply) {
+    const int i = prob % p.n_chunks;
+    return i * p.C + mt * BM < p.T;
+  }
+  return true;
+}
+
+// 32 fp32 values -> 32 bf16 stored at dst (16-byte aligned); columns past `valid` skipped
+// in groups of 8 (the column count is a multiple of 8).
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* v, int valid) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (q * 8 < valid) {
+      uint4 w;
+      w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+      w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+      w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+      w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      d4[q] = w;
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                   const __grid_constant__ CUtensorMap map_b1, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;                // [STAGES]
+  uint64_t* empty = bars + STAGES;      // [STAGES]
+  uint64_t* acc_full = bars + 2 * STAGES;   // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2]
+  uint64_t* drain = acc_empty + 2;          // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total_tiles = p.problems * p.m_tiles * p.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // producer state, kept at function scope for the drain after an abort
+  int p_stage = 0;
+  uint32_t p_phase = 0;
+  long p_issued = 0;
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b0);
+    if (KIND == kSwiglu) tma_prefetch_desc(&map_b1);
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int prob, mt, nt;
+      decode_tile(p, tile, prob, mt, nt);
+      if (!tile_active<KIND>(p, prob, mt)) continue;
+      bool ok = true;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!wait_bounded(&empty[p_stage], p_phase ^ 1u, p.st, abort_flag, 0x101)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + p_stage * STAGE_BYTES;
+        uint8_t* sb = sa + A_BYTES;
+        mbar_arrive_expect_tx(&full[p_stage], STAGE_BYTES);
+        const int k0 = kb * BK;
+        if (KIND == kSwiglu) {
+          tma_load_2d(sa, &map_a, &full[p_stage], k0, mt * BM);
+          tma_load_2d(sb, &map_b0, &full[p_stage], k0, nt * 128);
+          tma_load_2d(sb + B_BYTES / 2, &map_b1, &full[p_stage], k0, nt * 128);
+        } else if (KIND == kTarget) {
+          tma_load_2d(sa, &map_a, &full[p_stage], k0, mt * BM);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * (BK * 128), &map_b0, &full[p_stage], nt * BN + j * 64, k0);
+        } else {
+          const int b = prob / p.n_chunks;
+          const int i = prob - b * p.n_chunks;
+          tma_load_3d(sa, &map_a, &full[p_stage], k0, i * p.C + mt * BM, b);
+          tma_load_3d(sb, &map_b0, &full[p_stage], k0, nt * BN, prob);
+        }
+        ++p_issued;
+        if (++p_stage == STAGES) {
+          p_stage = 0;
+          p_phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, false, KIND == kTarget);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int prob, mt, nt;
+      decode_tile(p, tile, prob, mt, nt);
+      if (!tile_active<KIND>(p, prob, mt)) continue;
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, p.st, abort_flag, 0x102)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+      bool ok = true;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!wait_bounded(&full[stage], phase, p.st, abort_flag, 0x103)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t adesc = sdesc_sw128(a_addr + kk * 32, 16, 1024);
+          const uint64_t bdesc = (KIND == kTarget) ? sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024)
+                                                   : sdesc_sw128(b_addr + kk * 32, 16, 1024);
+          tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit(&acc_full[buf]);
+      ++it;
+    }
+  } else if (warp >= 2) {
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int prob, mt, nt;
+      decode_tile(p, tile, prob, mt, nt);
+      if (!tile_active<KIND>(p, prob, mt)) continue;
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!wait_bounded(&acc_full[buf], use & 1u, p.st, abort_flag, 0x104)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      if (KIND == kSwiglu) {
+        const int row = mt * BM + r_in_tile;
+        const bool row_ok = row < p.rows;
+        const int col0 = nt * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(t_row + c * 32, g);
+          tmem_ld32(t_row + 128 + c * 32, u);
+          tmem_ld_wait(g);
+          tmem_ld_wait(u);
+          float z[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float a = __uint_as_float(g[e]);
+            z[e] = a / (1.0f + __expf(-a)) * __uint_as_float(u[e]);
+          }
+          const int col = col0 + c * 32;
+          if (row_ok && col < p.cols) store32_bf16(p.out + (int64_t)row * p.out_ld + col, z, p.cols - col);
+        }
+      } else {
+        int row;
+        bool row_ok;
+        if (KIND == kApply) {
+          const int b = prob / p.n_chunks;
+          const int i = prob - b * p.n_chunks;
+          const int t = i * p.C + mt * BM + r_in_tile;
+          row_ok = t < p.T;
+          row = b * p.T + t;
+        } else {
+          row = mt * BM + r_in_tile;
+          row_ok = row < p.rows;
+        }
+        const int col0 = nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_row + c * 32, r);
+          tmem_ld_wait(r);
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * p.scale;
+          const int col = col0 + c * 32;
+          if (row_ok && col < p.cols) store32_bf16(p.out + (int64_t)row * p.out_ld + col, v, p.cols - col);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+      ++it;
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // Drain: wait (bounded) for this CTA's own MMAs and TMA copies still in flight.
+    if (warp == 1 && lane == 0) {
+      tc_commit(drain);
+      drain_wait(drain, 0, 50000000ull);
+    }
+    if (warp == 0 && lane == 0) {
+      for (long j = p_issued - 1; j >= 0 && j >= p_issued - STAGES; --j)
+        drain_wait(&full[j % STAGES], (uint32_t)((j / STAGES) & 1), 50000000ull);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace gemm
+}  // namespace ipttt

@@ -126,8 +126,10 @@ def make_inputs(w: Workload, T: int | None = None) -> dict:
         H, X0 = make_activations(w, b, T)
         Hs.append(H)
         Xs.append(X0)
-    out["H"] = torch.stack(Hs).contiguous()
-    out["X0"] = torch.stack(Xs).contiguous()
+    T_eff = w.T if T is None else T
+    dt = torch_dtype(w.dtype)
+    out["H"] = torch.stack(Hs).contiguous() if Hs else torch.empty((0, T_eff, w.d), dtype=dt)
+    out["X0"] = torch.stack(Xs).contiguous() if Xs else torch.empty((0, T_eff, w.d), dtype=dt)
     return out
 
 

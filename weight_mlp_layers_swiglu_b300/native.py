@@ -1,0 +1,304 @@
+"""ctypes binding of libipttt.so (include/ipttt.h).
+
+Argument marshalling only: torch tensors are checked for device, dtype, shape and
+contiguity, and their data pointers are passed to the C ABI together with the
+current CUDA stream.  Every step of the layer runs in the library's kernels; there
+is no Python or CPU fallback -- if the library is missing, load() raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+IPTTT_OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT"}
+F32, BF16 = 0, 1
+STAGES = ["swiglu", "conv", "target", "state", "apply"]
+
+_lib = None
+
+c_i64 = ctypes.c_int64
+c_vp = ctypes.c_void_p
+
+# name -> (restype, argtypes)
+_SIGNATURES = {
+    "ipttt_version": (ctypes.c_char_p, []),
+    "ipttt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "ipttt_create": (ctypes.c_int, [ctypes.POINTER(c_vp), ctypes.c_int, c_vp]),
+    "ipttt_set_stream": (ctypes.c_int, [c_vp, c_vp]),
+    "ipttt_set_wait_limit_ns": (ctypes.c_int, [c_vp, ctypes.c_uint64]),
+    "ipttt_sync": (ctypes.c_int, [c_vp]),
+    "ipttt_last_error": (ctypes.c_char_p, [c_vp]),
+    "ipttt_destroy": (None, [c_vp]),
+    "ipttt_workspace_size": (ctypes.c_int, [c_i64] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "ipttt_host_workspace_size": (ctypes.c_int,
+                                  [c_i64] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "ipttt_layer_forward": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                                                     c_vp, c_vp, c_vp, ctypes.c_size_t]),
+    "ipttt_layer_forward_host": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float,
+                                                                          ctypes.c_int, c_vp, c_vp, c_vp,
+                                                                          ctypes.c_size_t]),
+    "ipttt_swiglu": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, c_vp]),
+    "ipttt_target": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_int, c_vp, c_vp]),
+    "ipttt_chunk_state": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 5 + [ctypes.c_int, c_vp, c_vp]),
+    "ipttt_chunk_apply": (ctypes.c_int, [c_vp] * 3 + [c_i64] * 5 + [ctypes.c_int, c_vp]),
+    "ipttt_timing_begin": (ctypes.c_int, [c_vp]),
+    "ipttt_timing_read": (ctypes.c_int, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_i64),
+                                         ctypes.POINTER(c_i64)]),
+    "ipttt_layer_launches": (c_i64, [c_i64, c_i64, ctypes.c_int]),
+    "ipttt_selftest_wait_timeout": (ctypes.c_int, [c_vp]),
+    "ipttt_sm_count": (ctypes.c_int, [c_vp]),
+}
+
+
+def exported_symbols() -> list[str]:
+    return list(_SIGNATURES)
+
+
+def load(build_if_missing: bool = True):
+    """Load libipttt.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing:
+        _build.build()
+    if not os.path.exists(_build.LIB_PATH):
+        raise RuntimeError(f"CUDA library {_build.LIB_PATH} is missing; run weight_mlp_layers_swiglu_b300.build")
+    lib = ctypes.CDLL(_build.LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class IptttError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return BF16
+    if dt == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def workspace_size(B, T, d, d_ff, C, k, dtype: int, host: bool = False) -> int:
+    lib = load()
+    out = ctypes.c_size_t(0)
+    fn = lib.ipttt_host_workspace_size if host else lib.ipttt_workspace_size
+    st = fn(B, T, d, d_ff, C, k, dtype, ctypes.byref(out))
+    if st != IPTTT_OK:
+        raise IptttError(st, f"workspace_size(B={B}, T={T}, d={d}, d_ff={d_ff}, C={C}, k={k})")
+    return out.value
+
+
+def layer_launches(B, T, dtype: int) -> int:
+    return int(load().ipttt_layer_launches(B, T, dtype))
+
+
+def _ptr(t):
+    return c_vp(t.data_ptr()) if t is not None else c_vp(0)
+
+
+def _need(t: torch.Tensor, name: str, shape, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class Context:
+    """An ipttt context bound to a CUDA device and (by default) torch's current stream."""
+
+    def __init__(self, device: int | torch.device = 0, stream: torch.cuda.Stream | None = None):
+        self.lib = load()
+        dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        self.device = dev
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        h = c_vp(0)
+        st = self.lib.ipttt_create(ctypes.byref(h), dev.index or 0, c_vp(self.stream.cuda_stream))
+        if st != IPTTT_OK:
+            raise IptttError(st, "ipttt_create failed")
+        self.h = h
+        self._ws = None
+
+    def close(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            self.lib.ipttt_destroy(self.h)
+            self.h = c_vp(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, st: int, what: str):
+        if st != IPTTT_OK:
+            raise IptttError(st, f"{what}: {self.lib.ipttt_last_error(self.h).decode()}")
+
+    def set_stream(self, stream: torch.cuda.Stream):
+        self.stream = stream
+        self._check(self.lib.ipttt_set_stream(self.h, c_vp(stream.cuda_stream)), "set_stream")
+
+    def set_wait_limit_ns(self, ns: int):
+        self._check(self.lib.ipttt_set_wait_limit_ns(self.h, int(ns)), "set_wait_limit_ns")
+
+    def sync(self) -> int:
+        """Wait for the stream and return the device status (0 = OK); raises on CUDA errors."""
+        st = self.lib.ipttt_sync(self.h)
+        if st not in (IPTTT_OK, 5):
+            self._check(st, "sync")
+        return st
+
+    def last_error(self) -> str:
+        return self.lib.ipttt_last_error(self.h).decode()
+
+    @property
+    def sm_count(self) -> int:
+        return int(self.lib.ipttt_sm_count(self.h))
+
+    def workspace(self, B, T, d, d_ff, C, k, dtype: int, host: bool = False) -> torch.Tensor:
+        n = workspace_size(B, T, d, d_ff, C, k, dtype, host)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    # ------------------------------------------------------------------ the layer
+    def layer_forward(self, H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float,
+                      O=None, W_final=None, workspace=None):
+        """O [B,T,d] and the final fast weight W_final [B,d,d_ff] (fp32) of the layer."""
+        B, T, d = H.shape
+        f = W_gate.shape[0]
+        k = conv_w.shape[1]
+        dt, dev = H.dtype, self.device
+        for t, n, s in ((H, "H", (B, T, d)), (X0, "X0", (B, T, d)), (W_gate, "W_gate", (f, d)),
+                        (W_up, "W_up", (f, d)), (W_down0, "W_down0", (d, f)), (W_target, "W_target", (d, d)),
+                        (conv_w, "conv_w", (d, k))):
+            _need(t, n, s, dt, dev)
+        code = dtype_code(dt)
+        if O is None:
+            O = torch.empty((B, T, d), dtype=dt, device=dev)
+        if W_final is None:
+            W_final = torch.empty((B, d, f), dtype=torch.float32, device=dev)
+        _need(O, "O", (B, T, d), dt, dev)
+        _need(W_final, "W_final", (B, d, f), torch.float32, dev)
+        ws = workspace if workspace is not None else self.workspace(B, T, d, f, C, k, code)
+        st = self.lib.ipttt_layer_forward(self.h, _ptr(H), _ptr(X0), _ptr(W_gate), _ptr(W_up), _ptr(W_down0),
+                                          _ptr(W_target), _ptr(conv_w), B, T, d, f, C, k, float(eta), code,
+                                          _ptr(O), _ptr(W_final), _ptr(ws), ws.numel() * ws.element_size())
+        self._check(st, "layer_forward")
+        return O, W_final
+
+    def layer_forward_host(self, H_host, X0_host, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float,
+                           O_host, W_final_host, workspace=None):
+        """The layer with H, X0, O, W_final in (pinned) host memory; asynchronous until sync()."""
+        B, T, d = H_host.shape
+        f = W_gate.shape[0]
+        k = conv_w.shape[1]
+        dt, dev = W_gate.dtype, self.device
+        for t, n, s in ((W_gate, "W_gate", (f, d)), (W_up, "W_up", (f, d)), (W_down0, "W_down0", (d, f)),
+                        (W_target, "W_target", (d, d)), (conv_w, "conv_w", (d, k))):
+            _need(t, n, s, dt, dev)
+        cpu = torch.device("cpu")
+        _need(H_host, "H_host", (B, T, d), dt, cpu)
+        _need(X0_host, "X0_host", (B, T, d), dt, cpu)
+        _need(O_host, "O_host", (B, T, d), dt, cpu)
+        _need(W_final_host, "W_final_host", (B, d, f), torch.float32, cpu)
+        code = dtype_code(dt)
+        ws = workspace if workspace is not None else self.workspace(B, T, d, f, C, k, code, host=True)
+        st = self.lib.ipttt_layer_forward_host(self.h, _ptr(H_host), _ptr(X0_host), _ptr(W_gate), _ptr(W_up),
+                                               _ptr(W_down0), _ptr(W_target), _ptr(conv_w), B, T, d, f, C, k,
+                                               float(eta), code, _ptr(O_host), _ptr(W_final_host), _ptr(ws),
+                                               ws.numel() * ws.element_size())
+        self._check(st, "layer_forward_host")
+        return O_host, W_final_host
+
+    # ------------------------------------------------------------------ the steps
+    def swiglu(self, H2d, W_gate, W_up, Z=None):
+        rows, d = H2d.shape
+        f = W_gate.shape[0]
+        dt, dev = H2d.dtype, self.device
+        _need(H2d, "H", (rows, d), dt, dev)
+        _need(W_gate, "W_gate", (f, d), dt, dev)
+        _need(W_up, "W_up", (f, d), dt, dev)
+        if Z is None:
+            Z = torch.empty((rows, f), dtype=dt, device=dev)
+        _need(Z, "Z", (rows, f), dt, dev)
+        self._check(self.lib.ipttt_swiglu(self.h, _ptr(H2d), _ptr(W_gate), _ptr(W_up), rows, d, f, dtype_code(dt),
+                                          _ptr(Z)), "swiglu")
+        return Z
+
+    def target(self, X0, conv_w, W_target, scale: float = 1.0, V=None, Y=None):
+        B, T, d = X0.shape
+        k = conv_w.shape[1]
+        dt, dev = X0.dtype, self.device
+        _need(X0, "X0", (B, T, d), dt, dev)
+        _need(conv_w, "conv_w", (d, k), dt, dev)
+        _need(W_target, "W_target", (d, d), dt, dev)
+        if V is None:
+            V = torch.empty((B, T, d), dtype=dt, device=dev)
+        if Y is None:
+            Y = torch.empty((B, T, d), dtype=dt, device=dev)
+        self._check(self.lib.ipttt_target(self.h, _ptr(X0), _ptr(conv_w), _ptr(W_target), B, T, d, k, float(scale),
+                                          dtype_code(dt), _ptr(Y), _ptr(V)), "target")
+        return V, Y
+
+    def chunk_state(self, V, Z, W_down0, C: int, W_eff=None, W_final=None):
+        B, T, d = V.shape
+        f = Z.shape[2]
+        n = (T + C - 1) // C
+        dt, dev = V.dtype, self.device
+        _need(V, "V", (B, T, d), dt, dev)
+        _need(Z, "Z", (B, T, f), dt, dev)
+        _need(W_down0, "W_down0", (d, f), dt, dev)
+        if W_eff is None:
+            W_eff = torch.empty((B, n, d, f), dtype=dt, device=dev)
+        if W_final is None:
+            W_final = torch.empty((B, d, f), dtype=torch.float32, device=dev)
+        self._check(self.lib.ipttt_chunk_state(self.h, _ptr(V), _ptr(Z), _ptr(W_down0), B, T, d, f, C,
+                                               dtype_code(dt), _ptr(W_eff), _ptr(W_final)), "chunk_state")
+        return W_eff, W_final
+
+    def chunk_apply(self, Z, W_eff, C: int, O=None):
+        B, T, f = Z.shape
+        d = W_eff.shape[2]
+        n = (T + C - 1) // C
+        dt, dev = Z.dtype, self.device
+        _need(Z, "Z", (B, T, f), dt, dev)
+        _need(W_eff, "W_eff", (B, n, d, f), dt, dev)
+        if O is None:
+            O = torch.empty((B, T, d), dtype=dt, device=dev)
+        self._check(self.lib.ipttt_chunk_apply(self.h, _ptr(Z), _ptr(W_eff), B, T, d, f, C, dtype_code(dt),
+                                               _ptr(O)), "chunk_apply")
+        return O
+
+    # ------------------------------------------------------------------ measurement
+    def timing_begin(self):
+        self._check(self.lib.ipttt_timing_begin(self.h), "timing_begin")
+
+    def timing_read(self):
+        """Per-stage summed device ms, number of timed calls, kernels those calls launched."""
+        ms = (ctypes.c_double * len(STAGES))()
+        calls, launches = c_i64(0), c_i64(0)
+        self._check(self.lib.ipttt_timing_read(self.h, ms, ctypes.byref(calls), ctypes.byref(launches)),
+                    "timing_read")
+        return dict(zip(STAGES, list(ms))), calls.value, launches.value
+
+    def selftest_wait_timeout(self):
+        self._check(self.lib.ipttt_selftest_wait_timeout(self.h), "selftest_wait_timeout")
