@@ -1,0 +1,438 @@
+"""Throughput of the In-Place TTT fast-weight SwiGLU layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one call of the whole layer (SwiGLU, causal conv + target projection, chunk
+updates with their exclusive prefix, per-chunk apply) over one batch of the workload.  The
+default workload is the Qwen3-4B-shaped layer at 32k tokens (B=1, T=32768, d=2560,
+d_ff=9728, C=1024, k=4, eta=1/1024, bf16).  Inputs are seeded synthetic tensors, resident
+in HBM before the timed region; the per-step working set (~0.5 GB of inputs, ~2.6 GB of
+workspace) is larger than the 126 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own sequence of
+the workload (independent fast-weight states, no collective on the data path): weak scaling.
+
+--impl reference times the CPU oracle (float64 numpy, the repository's checker) on the
+host cores on a bounded sample of the same workload: its first 256 tokens per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s per In-Place-TTT MLP layer (4B shape, 32k ctx); % of BF16 tensor peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w) -> dict:
+    return {"workload": w.name, "B": w.B, "T": w.T, "d": w.d, "d_ff": w.d_ff, "C": w.C, "k": w.k,
+            "eta": w.eta, "l2": "inputs larger than L2 (no flush)"}
+
+
+def stage_flops(w) -> dict:
+    BT = w.B * w.T
+    return {"swiglu": 4.0 * BT * w.d * w.d_ff, "conv": 2.0 * BT * w.d * w.k, "target": 2.0 * BT * w.d * w.d,
+            "state": 2.0 * BT * w.d * w.d_ff, "apply": 2.0 * BT * w.d * w.d_ff}
+
+
+def stage_bytes(w) -> dict:
+    """Algorithmic HBM bytes per launch (each operand read once, each result written once)."""
+    es = 2 if w.dtype == "bf16" else 4
+    BT, d, f = w.B * w.T, w.d, w.d_ff
+    n = w.n_chunks
+    return {"swiglu": es * (BT * d + 2 * f * d + BT * f), "conv": es * (2 * BT * d + d * w.k),
+            "target": es * (2 * BT * d + d * d),
+            "state": es * (BT * d + BT * f + d * f + w.B * n * d * f) + 4 * w.B * d * f,
+            "apply": es * (BT * f + w.B * n * d * f + BT * d)}
+
+
+# ----------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (x itself when there is one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def sequence_of_rank(rank: int) -> int:
+    """Each rank runs its own sequence of the workload: sequence index = rank."""
+    return rank
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        # nvidia-smi numbers GPUs physically; map the CUDA ordinal through CUDA_VISIBLE_DEVICES
+        vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+        self.dev = vis[device_index] if device_index < len(vis) else str(device_index)
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != len(self.FIELDS):
+                    continue
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        load = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS runs the oracle's matrix products on."""
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = max((i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"), default=0)
+        if n:
+            return int(n)
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_sample(w, seconds: float = 15.0, min_chunks: int = 1):
+    """Time the CPU oracle on the first m chunks of the workload's first sequence (a causal prefix
+    is a complete layer call on its own).  m grows until ~`seconds` of CPU work."""
+    from oracle import oracle
+    from weight_mlp_layers_swiglu_b300.inputs import make_activations, make_weights
+
+    weights = make_weights(w)
+    m = min_chunks
+    tot_tokens, tot_time = 0, 0.0
+    while True:
+        T = min(m * w.C, w.T)
+        H, X0 = make_activations(w, 0, T)
+        t0 = time.perf_counter()
+        oracle.layer_forward(H[None], X0[None], weights["W_gate"], weights["W_up"], weights["W_down0"],
+                             weights["W_target"], weights["conv_w"], w.C, w.eta)
+        dt = time.perf_counter() - t0
+        tot_tokens, tot_time = T, dt
+        if dt * 2 > seconds or T >= w.T:
+            break
+        m *= 2
+    cores = blas_threads()
+    return {"value": tot_tokens / tot_time, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {tot_tokens} tokens ({tot_tokens // w.C} chunks) of sequence 0, full d/d_ff, "
+                      f"float64 numpy, {tot_time:.2f} s"}
+
+
+# ----------------------------------------------------------------------------- the reference arm
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import oracle
+    from weight_mlp_layers_swiglu_b300.inputs import make_activations, make_weights
+
+    weights = make_weights(w)
+    T = min(256, w.C, w.T)
+    H, X0 = make_activations(w, 0, T)
+
+    def step():
+        oracle.layer_forward(H[None], X0[None], weights["W_gate"], weights["W_up"], weights["W_down0"],
+                             weights["W_target"], weights["conv_w"], w.C, w.eta)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = T * args.steps / el
+    cores = blas_threads()
+    sample = f"first {T} tokens of sequence 0 per step (a causal prefix: one partial chunk), full d/d_ff, float64 numpy"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, w):
+    import torch
+
+    import weight_mlp_layers_swiglu_b300 as pkg
+    from weight_mlp_layers_swiglu_b300.inputs import make_activations, make_weights
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    # this rank's batch: the workload's own batch, sequences offset by rank * B
+    weights = {k: v.to(dev) for k, v in make_weights(w).items()}
+    Hs, Xs = [], []
+    for b in range(w.B):
+        H, X0 = make_activations(w, sequence_of_rank(rank) * w.B + b)
+        Hs.append(H)
+        Xs.append(X0)
+    H_host = torch.stack(Hs).contiguous()
+    X_host = torch.stack(Xs).contiguous()
+    H = H_host.to(dev)
+    X0 = X_host.to(dev)
+    ctx = pkg.Context(local)
+    stream = torch.cuda.current_stream(dev)
+    O = torch.empty((w.B, w.T, w.d), dtype=H.dtype, device=dev)
+    Wf = torch.empty((w.B, w.d, w.d_ff), dtype=torch.float32, device=dev)
+    ws = ctx.workspace(w.B, w.T, w.d, w.d_ff, w.C, w.k, pkg.dtype_code(H.dtype))
+
+    def step():
+        ctx.layer_forward(H, X0, weights["W_gate"], weights["W_up"], weights["W_down0"], weights["W_target"],
+                          weights["conv_w"], w.C, w.eta, O=O, W_final=Wf, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    st = ctx.sync()
+    if st != 0:
+        raise RuntimeError(f"device status {st} during warm-up: {ctx.last_error()}")
+
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ctx.timing_begin()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    ms_total = e0.elapsed_time(e1)
+    stage_ms, timed_calls, launches = ctx.timing_read()
+    st = ctx.sync()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region: {ctx.last_error()}")
+    ms_max = max_over_ranks(ms_total, world, dev)
+
+    e2e = None if args.no_e2e else e2e_leg(args, w, ctx, weights, H_host, X_host, dev, world)
+    if rank != 0:
+        return 0
+    finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks, e2e, H)
+    return 0
+
+
+def e2e_leg(args, w, ctx, weights, H_host, X_host, dev, world):
+    """The same metric end to end through the C ABI with host buffers: every step uploads H and
+    X0 from pinned memory, runs the layer and downloads O and W_final."""
+    import torch
+
+    import weight_mlp_layers_swiglu_b300 as pkg
+
+    stream = torch.cuda.current_stream(dev)
+    e2e_steps = max(3, min(args.steps, 10))
+    H_pin, X_pin = H_host.pin_memory(), X_host.pin_memory()
+    O_pin = torch.empty((w.B, w.T, w.d), dtype=H_host.dtype).pin_memory()
+    W_pin = torch.empty((w.B, w.d, w.d_ff), dtype=torch.float32).pin_memory()
+    ws_h = ctx.workspace(w.B, w.T, w.d, w.d_ff, w.C, w.k, pkg.dtype_code(H_host.dtype), host=True)
+
+    def step_host():
+        ctx.layer_forward_host(H_pin, X_pin, weights["W_gate"], weights["W_up"], weights["W_down0"],
+                               weights["W_target"], weights["conv_w"], w.C, w.eta, O_pin, W_pin, workspace=ws_h)
+
+    step_host()
+    ctx.sync()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    for _ in range(e2e_steps):
+        step_host()
+    h1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    if ctx.sync() != 0:
+        raise RuntimeError(f"device status in the e2e region: {ctx.last_error()}")
+    e2e_ms = max_over_ranks(h0.elapsed_time(h1), world, dev)
+    es = H_host.element_size()
+    h2d = 2 * w.B * w.T * w.d * es
+    d2h = w.B * w.T * w.d * es + w.B * w.d * w.d_ff * 4
+    return {"value": w.B * w.T * e2e_steps * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks, e2e, H):
+    import weight_mlp_layers_swiglu_b300 as pkg
+
+    peaks, peak_src = load_peaks()
+    fl = stage_flops(w)
+    by = stage_bytes(w)
+    per_launch = {s: stage_ms[s] / timed_calls for s in stage_ms}
+    kernels = {}
+    for s, ms in per_launch.items():
+        kernels[s] = {"ms": ms, "tflops": fl[s] / (ms * 1e-3) / 1e12, "hbm_gbs": by[s] / (ms * 1e-3) / 1e9}
+    dom = max(per_launch, key=per_launch.get)
+    ach = fl[dom] / (per_launch[dom] * 1e-3) / 1e12
+    traffic = dominant_traffic(dom, w)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback 1.8 PFLOP/s bf16 burst",
+                "algorithmic_flop_per_launch": fl[dom], "algorithmic_bytes_per_launch": by[dom]}
+    layer_tflops = w.flops() * args.steps * world / (ms_max * 1e-3) / 1e12
+    value = w.B * w.T * args.steps * world / (ms_max * 1e-3)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": workload_config(w) | {"parallelism": f"replicas x{world} (one sequence set per GPU)"},
+            "tflops": layer_tflops, "frac_bf16_peak": layer_tflops / peaks["bf16_tflops"] / world,
+            "frac_bf16_peak_sustained": layer_tflops / peaks["bf16_tflops_sustained"] / world,
+            "roofline": roofline, "kernels": kernels, "gpu_launches": launches * world if timed_calls == args.steps
+            else pkg.layer_launches(w.B, w.T, pkg.dtype_code(H.dtype)) * args.steps * world,
+            "e2e": e2e, "clocks": clocks.summary()}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = oracle_sample(w, seconds=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    ctx.close()
+
+
+def dominant_traffic(kernel: str, w):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu summary, if one
+    matches this workload and the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = t.get(w.name, {}).get(kernel)
+    if not entry:
+        return None
+    from weight_mlp_layers_swiglu_b300 import build as _b
+
+    if entry.get("source_digest") != source_digest(_b.SRC_DIR):
+        return None
+    return entry.get("bytes_per_launch")
+
+
+def source_digest(src_dir: str) -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src_dir)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(src_dir, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="qwen3_4b_32k")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (a shorter case of the same shapes, e.g. for profiler captures)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from weight_mlp_layers_swiglu_b300.inputs import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    if args.tokens is not None:
+        w = w.with_(name=f"{w.name}_T{args.tokens}", T=args.tokens)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
