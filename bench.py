@@ -357,10 +357,14 @@ def finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks,
     dom = max(per_launch, key=per_launch.get)
     ach = fl[dom] / (per_launch[dom] * 1e-3) / 1e12
     traffic = dominant_traffic(dom, w)
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
-                else "fallback 1.8 PFLOP/s bf16 burst",
+    # The kernels are timed inside a ~1 s loop of back-to-back layer calls, which runs into the
+    # board power limit: the sustained bf16 figure is the denominator (the burst one is reported too).
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback 1.4 PFLOP/s bf16 sustained",
+                "frac_of_burst": ach / peaks["bf16_tflops"],
                 "algorithmic_flop_per_launch": fl[dom], "algorithmic_bytes_per_launch": by[dom]}
     layer_tflops = w.flops() * args.steps * world / (ms_max * 1e-3) / 1e12
     value = w.B * w.T * args.steps * world / (ms_max * 1e-3)
