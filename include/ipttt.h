@@ -166,6 +166,47 @@ ipttt_status ipttt_chunk_state(ipttt_ctx* ctx, const void* V, const void* Z, con
 ipttt_status ipttt_chunk_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t B, int64_t T,
                                int64_t d, int64_t d_ff, int64_t C, ipttt_dtype dtype, void* O);
 
+/* ---- allocation-free variant ----
+ *
+ * The paper has no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory.  Examples: code that runs inside a host application whose device
+ * memory belongs to that application's own allocator or pool (and that therefore holds no
+ * right to call cudaMalloc), latency-critical loops where cudaMalloc / cudaFree could
+ * synchronise the device, and deployments whose device footprint must be fixed when the
+ * library is loaded.  Such callers cannot provide the Y scratch that ipttt_target needs.
+ */
+
+/* Size of the built-in scratch of ipttt_target_noalloc: 16 MiB of device memory that every
+ * GPU which loads this library reserves until the process exits.  The first 256 bytes hold
+ * a fallback status word; the rest holds the conv output Y. */
+#define IPTTT_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Step (2) exactly as ipttt_target computes it (same kernels, same results), but with the
+ * conv output Y kept in the library's built-in scratch instead of a caller buffer, and
+ * without a context.  It allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library call.
+ *   X0 [B,T,d], conv_w [d,k], W_target [d,d], V [B,T,d] (output), all `dtype`, device,
+ *   16-byte aligned.  V = scale * (CausalConv1D(X0) W_target).
+ *   status: optional device pointer to two uint32 words owned by the caller (zero them
+ *   before the first call); a device-side wait that runs past 2 s writes IPTTT_ERR_TIMEOUT
+ *   and a site code there.  With NULL a word inside the built-in scratch is used instead
+ *   and such a timeout is not reported.
+ *   cuda_stream: the stream to launch on (NULL = legacy default stream).
+ * Runs on the calling thread's current CUDA device.  The first call on each device sets
+ * up that device (looks up the scratch's device address with cudaGetSymbolAddress, finds
+ * the tensor-map encoder, sets kernel attributes): make that first call before any CUDA
+ * stream capture begins.  Later calls only launch two kernels.
+ * All calls share the one scratch, which keeps the last call's contents; nothing in it has
+ * to start at zero, because each call writes every element of Y it later reads.  Calls
+ * whose kernels may overlap on the GPU (other streams, or other host threads without
+ * ordering between them) race on the scratch and give wrong results: serialise them.
+ * Errors: INVALID_ARG (NULL / misaligned pointer, bad sizes), UNSUPPORTED (as
+ * ipttt_target), WORKSPACE when B*T*d*sizeof(dtype) > IPTTT_NOALLOC_SCRATCH_BYTES - 256
+ * (nothing is launched), CUDA. */
+ipttt_status ipttt_target_noalloc(const void* X0, const void* conv_w, const void* W_target, int64_t B,
+                                  int64_t T, int64_t d, int k, float scale, ipttt_dtype dtype, void* V,
+                                  uint32_t* status, void* cuda_stream);
+
 /* ---- measurement and self-test ---- */
 
 /* Start timing: later layer calls record a CUDA event at every stage boundary (up to 256

@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -851,3 +852,104 @@ ipttt_status ipttt_selftest_wait_timeout(ipttt_ctx* ctx) {
 int ipttt_sm_count(const ipttt_ctx* ctx) { return ctx ? ctx->sm_count : 0; }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free variant
+//
+// ipttt_target_noalloc: the target step for callers that cannot allocate device memory.  Its
+// scratch is this file-scope array, which the CUDA runtime places in every GPU that loads the
+// library.  In host code the name g_noalloc_scratch is only a host-side stand-in, so the
+// device address is looked up once per device with cudaGetSymbolAddress and passed to the
+// kernels.  Layout: [0, 256) fallback status word, [256, end) the conv output Y.
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[IPTTT_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr size_t kNoAllocStatusBytes = 256;
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+  bool ready = false;
+  uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on that device
+  EncodeTiledFn encode = nullptr;
+  int sm_count = 0;
+};
+
+NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// One-time set-up of the current device `dev` (which must be current).
+ipttt_status noalloc_device(int dev, NoAllocDevice* out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoAllocDevice& nd = g_noalloc_devices[dev];
+  if (!nd.ready) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+      cudaGetLastError();
+      return IPTTT_ERR_CUDA;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return IPTTT_ERR_CUDA;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      cudaGetLastError();
+      return IPTTT_ERR_CUDA;
+    }
+    ipttt_ctx probe;  // holds nothing on the device; only used to set the kernel attributes
+    probe.device = dev;
+    if (ensure_attrs(&probe) != IPTTT_OK) return IPTTT_ERR_CUDA;
+    nd.scratch = static_cast<uint8_t*>(addr);
+    nd.encode = reinterpret_cast<EncodeTiledFn>(fn);
+    nd.sm_count = sms;
+    nd.ready = true;
+  }
+  *out = nd;
+  return IPTTT_OK;
+}
+
+}  // namespace
+
+extern "C" ipttt_status ipttt_target_noalloc(const void* X0, const void* conv_w, const void* W_target, int64_t B,
+                                             int64_t T, int64_t d, int k, float scale, ipttt_dtype dtype, void* V,
+                                             uint32_t* status, void* cuda_stream) {
+  ipttt_status s = check_shape(nullptr, B, T, d, 8, 1, k, dtype, false);
+  if (s != IPTTT_OK) return s;
+  if (!std::isfinite(scale)) return IPTTT_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return IPTTT_OK;
+  if (!X0 || !conv_w || !W_target || !V || !aligned16(X0) || !aligned16(W_target) || !aligned16(V) ||
+      (status && (reinterpret_cast<uintptr_t>(status) & 3u)))
+    return IPTTT_ERR_INVALID_ARG;
+  const size_t y_bytes = (size_t)B * (size_t)T * (size_t)d * esize(dtype);
+  if (y_bytes > IPTTT_NOALLOC_SCRATCH_BYTES - kNoAllocStatusBytes) return IPTTT_ERR_WORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+    cudaGetLastError();
+    return IPTTT_ERR_CUDA;
+  }
+  NoAllocDevice nd;
+  if ((s = noalloc_device(dev, &nd)) != IPTTT_OK) return s;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  uint32_t* word = status;
+  if (word == nullptr) {
+    word = reinterpret_cast<uint32_t*>(nd.scratch);
+    if (cudaMemsetAsync(word, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess) {
+      cudaGetLastError();
+      return IPTTT_ERR_CUDA;
+    }
+  }
+  ipttt_ctx c;  // a view for the launchers: it owns no device memory and no events
+  c.device = dev;
+  c.stream = stream;
+  c.sm_count = nd.sm_count;
+  c.status = word;
+  c.encode = nd.encode;
+  c.attrs_set = true;
+  void* Y = nd.scratch + kNoAllocStatusBytes;
+  if ((s = run_conv(&c, X0, conv_w, B, T, d, k, dtype, Y)) != IPTTT_OK) return s;
+  return run_target_gemm(&c, Y, W_target, B * T, d, scale, dtype, V);
+}

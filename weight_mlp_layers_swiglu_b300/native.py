@@ -46,6 +46,8 @@ _SIGNATURES = {
     "ipttt_target": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_int, c_vp, c_vp]),
     "ipttt_chunk_state": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 5 + [ctypes.c_int, c_vp, c_vp]),
     "ipttt_chunk_apply": (ctypes.c_int, [c_vp] * 3 + [c_i64] * 5 + [ctypes.c_int, c_vp]),
+    "ipttt_target_noalloc": (ctypes.c_int, [c_vp] * 3 + [c_i64] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                                                    c_vp, c_vp, c_vp]),
     "ipttt_timing_begin": (ctypes.c_int, [c_vp]),
     "ipttt_timing_read": (ctypes.c_int, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_i64),
                                          ctypes.POINTER(c_i64)]),
