@@ -170,7 +170,8 @@ ipttt_status check_launch(ipttt_ctx* ctx, const char* what) {
 // ------------------------------------------------------------------ tensor maps
 
 bool encode_map(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                const uint64_t* strides_bytes, const uint32_t* box) {
+                const uint64_t* strides_bytes, const uint32_t* box,
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   cuuint64_t gd[3], gs[2];
   cuuint32_t bx[3], es[3];
   for (int i = 0; i < rank; ++i) {
@@ -180,7 +181,7 @@ bool encode_map(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int rank, cons
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
   const CUresult r =
-      ctx->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+      ctx->encode(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -206,6 +207,15 @@ bool map_3d(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int
   const uint64_t strides[2] = {(uint64_t)inner * 2, (uint64_t)inner * mid * 2};
   const uint32_t box[3] = {64, box_mid, 1};
   return encode_map(ctx, m, base, 3, dims, strides, box);
+}
+
+// [outer, mid, inner] fp32 row-major, box = 32 inner (128 bytes) x box_mid x 1.
+bool map_3d_f32(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int64_t mid, int64_t inner,
+                uint32_t box_mid) {
+  const uint64_t dims[3] = {(uint64_t)inner, (uint64_t)mid, (uint64_t)outer};
+  const uint64_t strides[2] = {(uint64_t)inner * 4, (uint64_t)inner * mid * 4};
+  const uint32_t box[3] = {32, box_mid, 1};
+  return encode_map(ctx, m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
 ipttt_status ensure_attrs(ipttt_ctx* ctx) {
@@ -345,8 +355,10 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
   const int64_t n = n_chunks_of(T, C);
   if (B == 0 || n == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
-    CUtensorMap mv, mz;
-    if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64)) return IPTTT_ERR_CUDA;
+    CUtensorMap mv, mz, mw, mf;
+    if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64) ||
+        !map_3d(ctx, &mw, W_eff, B * n, d, f, 32) || !map_3d_f32(ctx, &mf, W_final, B, d, f, 32))
+      return IPTTT_ERR_CUDA;
     state::Params p{};
     p.B = (int)B;
     p.T = (int)T;
@@ -358,12 +370,10 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
     p.n_units = ceil_div(f, state::BNF);
     p.units = (int)(B * p.m_units * p.n_units);
     p.W0 = static_cast<const __nv_bfloat16*>(W0);
-    p.W_eff = static_cast<__nv_bfloat16*>(W_eff);
-    p.W_final = W_final;
     p.st = dev_status(ctx);
     const int pairs = (p.units + 1) / 2;
     const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
-    state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, p);
+    state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, mw, mf, p);
     return check_launch(ctx, "state launch");
   }
   (void)split_timing;

@@ -32,16 +32,78 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+// Output staging: each epilogue warp owns two 4 KB boxes (32 rows x 128 B, 128-byte swizzle)
+// that alternate between TMA tensor stores.
+constexpr int OUT_BOX_BYTES = 32 * 128;
+constexpr int OUT_BYTES = 4 * 2 * OUT_BOX_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + BAR_BYTES;
 
 struct Params {
   int B, T, d, f, C, n_chunks;
   int m_units, n_units, units;  // units = B * n_units * m_units
-  const __nv_bfloat16* W0;      // [d, f]
-  __nv_bfloat16* W_eff;         // [B, n_chunks, d, f]
-  float* W_final;               // [B, d, f]
+  const __nv_bfloat16* W0;      // [d, f]; W_eff [B, n_chunks, d, f] and W_final [B, d, f] via tensor maps
   DevStatus st;
 };
+
+// Per-warp staging of 32 rows x 128 bytes for TMA tensor stores.  Row r of the box sits at
+// r * 128 with its 16-byte chunks permuted by the 128-byte swizzle (chunk j -> j ^ (r & 7)),
+// which both matches the tensor map and keeps the shared-memory writes conflict free.
+struct OutStager {
+  uint8_t* buf;  // two OUT_BOX_BYTES boxes, 1024-byte aligned
+  uint32_t seq;
+  int lane;
+
+  // All 32 lanes call this with their row's 128 bytes; lane 0 issues the store.
+  __device__ __forceinline__ void put(const uint32_t (&row)[32], const CUtensorMap* map, int x, int y, int z) {
+    uint8_t* box = buf + (seq & 1u) * OUT_BOX_BYTES;
+    if (lane == 0 && seq >= 2) bulk_wait_read<1>();  // the store that last used this box has read it
+    __syncwarp();
+    const uint32_t base = smem_u32(box) + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(base + (uint32_t)((j ^ (lane & 7)) << 4), row[4 * j], row[4 * j + 1], row[4 * j + 2],
+                   row[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(map, box, x, y, z);
+      bulk_commit();
+    }
+    ++seq;
+  }
+};
+
+// Reads the 256 accumulator columns of this thread's TMEM lane and stores them as bf16
+// W_eff rows (4 boxes of 64 columns) for state rows y.. y+31 of slice z.
+__device__ __forceinline__ void snapshot_bf16(OutStager& out, uint32_t t_row, const CUtensorMap* map, int x0, int y,
+                                              int z) {
+#pragma unroll 1
+  for (int g = 0; g < BNF / 64; ++g) {
+    uint32_t a[32], b[32], row[32];
+    tmem_ld32(t_row + g * 64, a);
+    tmem_ld32(t_row + g * 64 + 32, b);
+    tmem_ld_wait(a);
+    tmem_ld_wait(b);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      row[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+      row[16 + e] = pack_bf16x2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
+    }
+    out.put(row, map, x0 + g * 64, y, z);
+  }
+}
+
+// The same for the fp32 final state (8 boxes of 32 columns).
+__device__ __forceinline__ void snapshot_f32(OutStager& out, uint32_t t_row, const CUtensorMap* map, int x0, int y,
+                                             int z) {
+#pragma unroll 1
+  for (int g = 0; g < BNF / 32; ++g) {
+    uint32_t a[32];
+    tmem_ld32(t_row + g * 32, a);
+    tmem_ld_wait(a);
+    out.put(a, map, x0 + g * 32, y, z);
+  }
+}
 
 // Unit order: d-tile fastest, so that concurrently running CTAs share the same Z columns.
 __device__ __forceinline__ void decode_unit(const Params& p, int u, int& b, int& mb, int& nb) {
@@ -58,10 +120,12 @@ __device__ __forceinline__ int chunk_kblocks(const Params& p, int i) {
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_state_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_z,
+                    const __grid_constant__ CUtensorMap map_weff, const __grid_constant__ CUtensorMap map_wfin,
                     const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* out_stage = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + OUT_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* chunk_done = bars + 2 * STAGES;  // [2]  MMA -> epilogue: chunk's MMAs finished
@@ -183,10 +247,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= 2) {
     const int q = warp & 3;
     const int r_in_tile = q * 32 + lane;
+    OutStager out{out_stage + (warp - 2) * 2 * OUT_BOX_BYTES, 0u, lane};
+    tma_prefetch_desc(&map_weff);
+    tma_prefetch_desc(&map_wfin);
     uint32_t chunk_waits[2] = {0, 0};
     bool ok = true;
     for (int pr = blockIdx.x; pr < pairs && ok; pr += gridDim.x) {
-      // initialise both accumulators with W_down0 and emit W_eff[0] = W_down0
+      // initialise both accumulators with W_down0; the snapshot right after emits W_eff[0] = W_down0
       for (int slot = 0; slot < 2; ++slot) {
         const int u = 2 * pr + slot;
         if (u >= p.units) break;
@@ -196,7 +263,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool row_ok = row < p.d;
         const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BNF);
         const __nv_bfloat16* src = p.W0 + (int64_t)row * p.f;
-        __nv_bfloat16* dst = p.W_eff + ((int64_t)b * p.n_chunks * p.d + row) * p.f;
 #pragma unroll 1
         for (int c = 0; c < BNF / 32; ++c) {
           const int col = nb * BNF + c * 32;
@@ -204,10 +270,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_ok && col + g * 8 < p.f) {
-              w = *reinterpret_cast<const uint4*>(src + col + g * 8);
-              if (p.n_chunks > 0) *reinterpret_cast<uint4*>(dst + col + g * 8) = w;
-            }
+            if (row_ok && col + g * 8 < p.f) w = *reinterpret_cast<const uint4*>(src + col + g * 8);
             r[g * 8 + 0] = __float_as_uint(bf16_lo(w.x));
             r[g * 8 + 1] = __float_as_uint(bf16_hi(w.x));
             r[g * 8 + 2] = __float_as_uint(bf16_lo(w.y));
@@ -220,6 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_st32(t_row + c * 32, r);
         }
         tmem_st_wait();
+        snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks);
         tc_fence_before();
         mbar_arrive(&snap_done[slot]);
       }
@@ -236,60 +300,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           int b, mb, nb;
           decode_unit(p, u, b, mb, nb);
-          const int row = mb * BMD + r_in_tile;
-          const bool row_ok = row < p.d;
           const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BNF);
           if (i < p.n_chunks) {
-            __nv_bfloat16* dst = p.W_eff + (((int64_t)b * p.n_chunks + i) * p.d + row) * p.f;
-#pragma unroll 1
-            for (int c = 0; c < BNF / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(t_row + c * 32, r);
-              tmem_ld_wait(r);
-              const int col = nb * BNF + c * 32;
-              if (row_ok && col < p.f) {
-                float v[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-                uint4* d4 = reinterpret_cast<uint4*>(dst + col);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                  if (col + g * 8 < p.f) {
-                    uint4 w;
-                    w.x = pack_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
-                    w.y = pack_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
-                    w.z = pack_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
-                    w.w = pack_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
-                    d4[g] = w;
-                  }
-                }
-              }
-            }
+            snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks + i);
             tc_fence_before();
             mbar_arrive(&snap_done[slot]);
           } else {
-            float* dst = p.W_final + ((int64_t)b * p.d + row) * p.f;
-#pragma unroll 1
-            for (int c = 0; c < BNF / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(t_row + c * 32, r);
-              tmem_ld_wait(r);
-              const int col = nb * BNF + c * 32;
-              if (row_ok && col < p.f) {
-                float4* d4 = reinterpret_cast<float4*>(dst + col);
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                  if (col + g * 4 < p.f)
-                    d4[g] = make_float4(__uint_as_float(r[g * 4 + 0]), __uint_as_float(r[g * 4 + 1]),
-                                        __uint_as_float(r[g * 4 + 2]), __uint_as_float(r[g * 4 + 3]));
-                }
-              }
-            }
+            snapshot_f32(out, t_row, &map_wfin, nb * BNF, mb * BMD + q * 32, b);
             tc_fence_before();
           }
         }
       }
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   __syncthreads();
