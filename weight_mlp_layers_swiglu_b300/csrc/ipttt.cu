@@ -247,9 +247,9 @@ ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const voi
                         int64_t f, ipttt_dtype dt, void* Z) {
   if (rows == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
-    CUtensorMap ma, mb0, mb1;
+    CUtensorMap ma, mb0, mb1, mo;
     if (!map_2d(ctx, &ma, H, rows, d, 64, 128) || !map_2d(ctx, &mb0, Wg, f, d, 64, 128) ||
-        !map_2d(ctx, &mb1, Wu, f, d, 64, 128))
+        !map_2d(ctx, &mb1, Wu, f, d, 64, 128) || !map_2d(ctx, &mo, Z, rows, f, 64, 32))
       return IPTTT_ERR_CUDA;
     gemm::Params p{};
     p.m_tiles = ceil_div(rows, gemm::BM);
@@ -257,15 +257,12 @@ ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const voi
     p.k_blocks = ceil_div(d, gemm::BK);
     p.problems = 1;
     p.group_m = 16;
-    p.out = static_cast<__nv_bfloat16*>(Z);
-    p.out_ld = f;
-    p.rows = (int)rows;
-    p.cols = (int)f;
     p.scale = 1.f;
     p.st = dev_status(ctx);
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-    gemm::tc_gemm_kernel<gemm::kSwiglu><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb0, mb1, p);
+    gemm::tc_gemm_kernel<gemm::kSwiglu><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb0, mb1, mo,
+                                                                                                    p);
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(H);
@@ -315,23 +312,21 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
                              ipttt_dtype dt, void* V) {
   if (rows == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
-    CUtensorMap ma, mb;
-    if (!map_2d(ctx, &ma, Y, rows, d, 64, 128) || !map_2d(ctx, &mb, Wt, d, d, 64, 64)) return IPTTT_ERR_CUDA;
+    CUtensorMap ma, mb, mo;
+    if (!map_2d(ctx, &ma, Y, rows, d, 64, 128) || !map_2d(ctx, &mb, Wt, d, d, 64, 64) ||
+        !map_2d(ctx, &mo, V, rows, d, 64, 32))
+      return IPTTT_ERR_CUDA;
     gemm::Params p{};
     p.m_tiles = ceil_div(rows, gemm::BM);
     p.n_tiles = ceil_div(d, gemm::BN);
     p.k_blocks = ceil_div(d, gemm::BK);
     p.problems = 1;
     p.group_m = 16;
-    p.out = static_cast<__nv_bfloat16*>(V);
-    p.out_ld = d;
-    p.rows = (int)rows;
-    p.cols = (int)d;
     p.scale = scale;
     p.st = dev_status(ctx);
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-    gemm::tc_gemm_kernel<gemm::kTarget><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, p);
+    gemm::tc_gemm_kernel<gemm::kTarget><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, mo, p);
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(Y);
@@ -349,9 +344,11 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
 }
 
 // Steps (3)+(4).  fp32: Step 1 (all Delta_i) then Step 2 (scan); bf16: one fused kernel.
+// skip_first (bf16): leave W_eff[b, 0] (= W_down0) unwritten; the layer's apply then reads
+// W_down0 for chunk 0 directly.
 ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
                        int64_t d, int64_t f, int64_t C, ipttt_dtype dt, void* W_eff, float* W_final,
-                       bool split_timing = false, int call = -1) {
+                       bool skip_first = false) {
   const int64_t n = n_chunks_of(T, C);
   if (B == 0 || n == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
@@ -370,14 +367,13 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
     p.n_units = ceil_div(f, state::BNF);
     p.units = (int)(B * p.m_units * p.n_units);
     p.W0 = static_cast<const __nv_bfloat16*>(W0);
+    p.skip_first = skip_first ? 1 : 0;
     p.st = dev_status(ctx);
     const int pairs = (p.units + 1) / 2;
     const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
     state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, mw, mf, p);
     return check_launch(ctx, "state launch");
   }
-  (void)split_timing;
-  (void)call;
   simt::SgemmParams p{};
   p.A = static_cast<const float*>(V);
   p.B = static_cast<const float*>(Z);
@@ -402,29 +398,34 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
   return check_launch(ctx, "scan launch");
 }
 
+// W0 (bf16, optional): chunk 0 of every sequence is applied with W0 instead of W_eff[b, 0].
 ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t B, int64_t T, int64_t d, int64_t f,
-                       int64_t C, ipttt_dtype dt, void* O) {
+                       int64_t C, ipttt_dtype dt, void* O, const void* W0 = nullptr) {
   const int64_t n = n_chunks_of(T, C);
   if (B == 0 || n == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
-    CUtensorMap ma, mb;
-    if (!map_3d(ctx, &ma, Z, B, T, f, 128) || !map_3d(ctx, &mb, W_eff, B * n, d, f, 256)) return IPTTT_ERR_CUDA;
+    CUtensorMap ma, mb, mw0, mo;
+    if (!map_3d(ctx, &ma, Z, B, T, f, 128) || !map_3d(ctx, &mb, W_eff, B * n, d, f, 256) ||
+        !map_3d(ctx, &mo, O, B, T, d, 32))
+      return IPTTT_ERR_CUDA;
+    if (W0 != nullptr) {
+      if (!map_2d(ctx, &mw0, W0, d, f, 64, 256)) return IPTTT_ERR_CUDA;
+    } else {
+      mw0 = mb;
+    }
     gemm::Params p{};
     p.m_tiles = (int)(C / gemm::BM);
     p.n_tiles = ceil_div(d, gemm::BN);
     p.k_blocks = ceil_div(f, gemm::BK);
     p.problems = (int)(B * n);
     p.group_m = 16;
-    p.out = static_cast<__nv_bfloat16*>(O);
-    p.out_ld = d;
-    p.rows = (int)T;
-    p.cols = (int)d;
     p.scale = 1.f;
     p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
+    p.first_from_w0 = W0 != nullptr ? 1 : 0;
     p.st = dev_status(ctx);
     const int tiles = p.problems * p.m_tiles * p.n_tiles;
     const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-    gemm::tc_gemm_kernel<gemm::kApply><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, p);
+    gemm::tc_gemm_kernel<gemm::kApply><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mw0, mo, p);
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(Z);
@@ -481,9 +482,10 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   mark(ctx, call, 2);
   if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V)) != IPTTT_OK) return s;
   mark(ctx, call, 3);
-  if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final)) != IPTTT_OK) return s;
+  const bool bf16 = dt == IPTTT_BF16;  // W_eff[b, 0] = W_down0: the apply reads W_down0 itself
+  if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, bf16)) != IPTTT_OK) return s;
   mark(ctx, call, 4);
-  if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O)) != IPTTT_OK) return s;
+  if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, bf16 ? W0 : nullptr)) != IPTTT_OK) return s;
   mark(ctx, call, 5);
   if (call >= 0) ctx->timed_launches += ipttt_layer_launches(B, T, dt);
   return IPTTT_OK;

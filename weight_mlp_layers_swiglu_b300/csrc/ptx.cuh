@@ -127,6 +127,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's bulk groups still read shared memory.
@@ -254,6 +261,53 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ----------------------------------------------------------------- output staging
+
+// Per-warp staging of 32 rows x 128 bytes for TMA tensor stores.  Row r of the box sits at
+// r * 128 with its 16-byte chunks permuted by the 128-byte swizzle (chunk j -> j ^ (r & 7)),
+// which both matches the tensor map and keeps the shared-memory writes conflict free.  Two
+// boxes alternate, so filling one overlaps the store of the other.
+constexpr int OUT_BOX_BYTES = 32 * 128;
+
+struct OutStager {
+  uint8_t* buf;  // two OUT_BOX_BYTES boxes, 1024-byte aligned
+  uint32_t seq;
+  int lane;
+
+  // All 32 lanes call this with their row's 128 bytes; returns the filled box (lane 0 then
+  // issues the store through store2d / store3d).
+  __device__ __forceinline__ uint8_t* fill(const uint32_t (&row)[32]) {
+    uint8_t* box = buf + (seq & 1u) * OUT_BOX_BYTES;
+    if (lane == 0 && seq >= 2) bulk_wait_read<1>();  // the store that last used this box has read it
+    __syncwarp();
+    const uint32_t base = smem_u32(box) + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(base + (uint32_t)((j ^ (lane & 7)) << 4), row[4 * j], row[4 * j + 1], row[4 * j + 2],
+                   row[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    ++seq;
+    return box;
+  }
+
+  __device__ __forceinline__ void put(const uint32_t (&row)[32], const CUtensorMap* map, int x, int y, int z) {
+    uint8_t* box = fill(row);
+    if (lane == 0) {
+      tma_store_3d(map, box, x, y, z);
+      bulk_commit();
+    }
+  }
+
+  __device__ __forceinline__ void put(const uint32_t (&row)[32], const CUtensorMap* map, int x, int y) {
+    uint8_t* box = fill(row);
+    if (lane == 0) {
+      tma_store_2d(map, box, x, y);
+      bulk_commit();
+    }
+  }
+};
 
 // ----------------------------------------------------------------- small helpers
 

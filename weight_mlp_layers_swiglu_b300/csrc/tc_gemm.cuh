@@ -7,7 +7,8 @@
 //               TMEM accumulators (2 x 256 fp32 columns), so the epilogue of one
 //               tile overlaps the main loop of the next.
 //   warps 2-5   epilogue: tcgen05.ld the accumulator (one TMEM lane = one output
-//               row per thread), apply the step's epilogue, store bf16 to HBM.
+//               row per thread), apply the step's epilogue, stage 32 x 64 bf16 boxes
+//               in swizzled shared memory and write them with TMA tensor stores.
 //
 // The same kernel serves three steps of the layer (zhichai.net "In-Place TTT：给LLM装上
 // "临时记忆插槽"，让它边读边学"):
@@ -18,7 +19,8 @@
 //           by the conv kernel).  W_target is [d_in, d_out], so B is MN-major.
 //   Apply   §3.2 Step 3:      O_i = Z_i W_eff[i]^T for every chunk i of every sequence;
 //           the problem index selects the chunk's rows of Z and its slice of the
-//           W_eff stack (3-D tensor maps).
+//           W_eff stack (3-D tensor maps); chunk 0 may read W_down0 directly, since
+//           W_eff[0] = W_down0.
 #pragma once
 
 #include "ptx.cuh"
@@ -36,7 +38,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+constexpr int OUT_BYTES = 4 * 2 * OUT_BOX_BYTES;  // two staging boxes per epilogue warp
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + BAR_BYTES;
 
 enum Kind : int { kSwiglu = 0, kTarget = 1, kApply = 2 };
 
@@ -44,12 +47,9 @@ struct Params {
   int m_tiles, n_tiles, k_blocks;  // per problem
   int problems;                    // Apply: B * n_chunks, else 1
   int group_m;                     // rasterisation: m-tiles per group
-  __nv_bfloat16* out;
-  int64_t out_ld;  // elements between output rows
-  int rows;        // valid output rows: B*T (Swiglu, Target) or T (Apply, per sequence)
-  int cols;        // valid output columns
   float scale;
   int T, C, n_chunks;  // Apply only
+  int first_from_w0;   // Apply: chunk 0 of each sequence reads W_down0 (map_b1) instead of the stack
   DevStatus st;
 };
 
@@ -74,30 +74,15 @@ __device__ __forceinline__ bool tile_active(const Params& p, int prob, int mt) {
   return true;
 }
 
-// 32 fp32 values -> 32 bf16 stored at dst (16-byte aligned); columns past `valid` skipped
-// in groups of 8 (the column count is a multiple of 8).
-__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* v, int valid) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (q * 8 < valid) {
-      uint4 w;
-      w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-      w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-      w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-      w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-      d4[q] = w;
-    }
-  }
-}
-
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
-                   const __grid_constant__ CUtensorMap map_b1, const Params p) {
+                   const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_out,
+                   const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* out_stage = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + OUT_BYTES);
   uint64_t* full = bars;                // [STAGES]
   uint64_t* empty = bars + STAGES;      // [STAGES]
   uint64_t* acc_full = bars + 2 * STAGES;   // [2]
@@ -140,7 +125,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b0);
-    if (KIND == kSwiglu) tma_prefetch_desc(&map_b1);
+    if (KIND != kTarget) tma_prefetch_desc(&map_b1);
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int prob, mt, nt;
       decode_tile(p, tile, prob, mt, nt);
@@ -167,7 +152,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int b = prob / p.n_chunks;
           const int i = prob - b * p.n_chunks;
           tma_load_3d(sa, &map_a, &full[p_stage], k0, i * p.C + mt * BM, b);
-          tma_load_3d(sb, &map_b0, &full[p_stage], k0, nt * BN, prob);
+          if (i == 0 && p.first_from_w0)
+            tma_load_2d(sb, &map_b1, &full[p_stage], k0, nt * BN);
+          else
+            tma_load_3d(sb, &map_b0, &full[p_stage], k0, nt * BN, prob);
         }
         ++p_issued;
         if (++p_stage == STAGES) {
@@ -219,7 +207,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int r_in_tile = q * 32 + lane;
+    OutStager out{out_stage + (warp - 2) * 2 * OUT_BOX_BYTES, 0u, lane};
+    tma_prefetch_desc(&map_out);
     int it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int prob, mt, nt;
@@ -231,55 +220,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
       if (KIND == kSwiglu) {
-        const int row = mt * BM + r_in_tile;
-        const bool row_ok = row < p.rows;
-        const int col0 = nt * 128;
+        // 128 output columns: two boxes of 64, each from 64 gate and 64 up accumulator columns
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld32(t_row + c * 32, g);
-          tmem_ld32(t_row + 128 + c * 32, u);
-          tmem_ld_wait(g);
-          tmem_ld_wait(u);
-          float z[32];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t row[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float a = __uint_as_float(g[e]);
-            z[e] = a / (1.0f + __expf(-a)) * __uint_as_float(u[e]);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t g[32], u[32];
+            tmem_ld32(t_row + h * 64 + c * 32, g);
+            tmem_ld32(t_row + 128 + h * 64 + c * 32, u);
+            tmem_ld_wait(g);
+            tmem_ld_wait(u);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float a0 = __uint_as_float(g[2 * e]), a1 = __uint_as_float(g[2 * e + 1]);
+              const float z0 = a0 / (1.0f + __expf(-a0)) * __uint_as_float(u[2 * e]);
+              const float z1 = a1 / (1.0f + __expf(-a1)) * __uint_as_float(u[2 * e + 1]);
+              row[c * 16 + e] = pack_bf16x2(z0, z1);
+            }
           }
-          const int col = col0 + c * 32;
-          if (row_ok && col < p.cols) store32_bf16(p.out + (int64_t)row * p.out_ld + col, z, p.cols - col);
+          out.put(row, &map_out, nt * 128 + h * 64, mt * BM + q * 32);
         }
       } else {
-        int row;
-        bool row_ok;
-        if (KIND == kApply) {
-          const int b = prob / p.n_chunks;
-          const int i = prob - b * p.n_chunks;
-          const int t = i * p.C + mt * BM + r_in_tile;
-          row_ok = t < p.T;
-          row = b * p.T + t;
-        } else {
-          row = mt * BM + r_in_tile;
-          row_ok = row < p.rows;
-        }
-        const int col0 = nt * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t_row + c * 32, r);
-          tmem_ld_wait(r);
-          float v[32];
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t a[32], b[32], row[32];
+          tmem_ld32(t_row + h * 64, a);
+          tmem_ld32(t_row + h * 64 + 32, b);
+          tmem_ld_wait(a);
+          tmem_ld_wait(b);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * p.scale;
-          const int col = col0 + c * 32;
-          if (row_ok && col < p.cols) store32_bf16(p.out + (int64_t)row * p.out_ld + col, v, p.cols - col);
+          for (int e = 0; e < 16; ++e) {
+            row[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
+            row[16 + e] = pack_bf16x2(__uint_as_float(b[2 * e]) * p.scale, __uint_as_float(b[2 * e + 1]) * p.scale);
+          }
+          if (KIND == kApply) {
+            const int bq = prob / p.n_chunks;
+            const int i = prob - bq * p.n_chunks;
+            out.put(row, &map_out, nt * BN + h * 64, i * p.C + mt * BM + q * 32, bq);
+          } else {
+            out.put(row, &map_out, nt * BN + h * 64, mt * BM + q * 32);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
       ++it;
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   __syncthreads();

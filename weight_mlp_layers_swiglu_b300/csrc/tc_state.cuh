@@ -34,7 +34,6 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 // Output staging: each epilogue warp owns two 4 KB boxes (32 rows x 128 B, 128-byte swizzle)
 // that alternate between TMA tensor stores.
-constexpr int OUT_BOX_BYTES = 32 * 128;
 constexpr int OUT_BYTES = 4 * 2 * OUT_BOX_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + BAR_BYTES;
 
@@ -42,35 +41,8 @@ struct Params {
   int B, T, d, f, C, n_chunks;
   int m_units, n_units, units;  // units = B * n_units * m_units
   const __nv_bfloat16* W0;      // [d, f]; W_eff [B, n_chunks, d, f] and W_final [B, d, f] via tensor maps
+  int skip_first;               // 1: W_eff[b, 0] (= W_down0) is not written (the apply reads W_down0)
   DevStatus st;
-};
-
-// Per-warp staging of 32 rows x 128 bytes for TMA tensor stores.  Row r of the box sits at
-// r * 128 with its 16-byte chunks permuted by the 128-byte swizzle (chunk j -> j ^ (r & 7)),
-// which both matches the tensor map and keeps the shared-memory writes conflict free.
-struct OutStager {
-  uint8_t* buf;  // two OUT_BOX_BYTES boxes, 1024-byte aligned
-  uint32_t seq;
-  int lane;
-
-  // All 32 lanes call this with their row's 128 bytes; lane 0 issues the store.
-  __device__ __forceinline__ void put(const uint32_t (&row)[32], const CUtensorMap* map, int x, int y, int z) {
-    uint8_t* box = buf + (seq & 1u) * OUT_BOX_BYTES;
-    if (lane == 0 && seq >= 2) bulk_wait_read<1>();  // the store that last used this box has read it
-    __syncwarp();
-    const uint32_t base = smem_u32(box) + (uint32_t)lane * 128u;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      st_shared_v4(base + (uint32_t)((j ^ (lane & 7)) << 4), row[4 * j], row[4 * j + 1], row[4 * j + 2],
-                   row[4 * j + 3]);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_3d(map, box, x, y, z);
-      bulk_commit();
-    }
-    ++seq;
-  }
 };
 
 // Reads the 256 accumulator columns of this thread's TMEM lane and stores them as bf16
@@ -283,7 +255,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_st32(t_row + c * 32, r);
         }
         tmem_st_wait();
-        snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks);
+        if (!p.skip_first) snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks);
         tc_fence_before();
         mbar_arrive(&snap_done[slot]);
       }
