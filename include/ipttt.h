@@ -59,10 +59,12 @@ typedef enum {
 
 typedef enum { IPTTT_F32 = 0, IPTTT_BF16 = 1 } ipttt_dtype;
 
-/* Kernel stages, in launch order, as reported by ipttt_timing_read(). */
+/* Kernel stages as reported by ipttt_timing_read().  The causal conv runs on an internal
+ * side stream, forked from and joined back into the context's stream, and overlaps the
+ * SwiGLU GEMM; its time is measured on that side stream. */
 typedef enum {
   IPTTT_STAGE_SWIGLU = 0, /* step (1)                                     */
-  IPTTT_STAGE_CONV = 1,   /* causal conv of step (2)                      */
+  IPTTT_STAGE_CONV = 1,   /* causal conv of step (2), overlapping (1)     */
   IPTTT_STAGE_TARGET = 2, /* W_target projection of step (2), times eta   */
   IPTTT_STAGE_STATE = 3,  /* steps (3)+(4): chunk updates and prefix      */
   IPTTT_STAGE_APPLY = 4,  /* step (5)                                     */
@@ -76,8 +78,9 @@ const char* ipttt_version(void);
 const char* ipttt_status_string(ipttt_status s);
 
 /* Create a context on CUDA device `device`, bound to `cuda_stream` (a cudaStream_t; NULL =
- * the legacy default stream).  Allocates a 8-byte device status word and CUDA events; this
- * is the only call that allocates device memory.  *out receives the context.
+ * the legacy default stream).  Allocates a 8-byte device status word, CUDA events and one
+ * internal side stream (ordered after and joined back into the context's stream by events);
+ * this is the only call that allocates device memory.  *out receives the context.
  * Errors: INVALID_ARG (out == NULL, bad device), CUDA. */
 ipttt_status ipttt_create(ipttt_ctx** out, int device, void* cuda_stream);
 

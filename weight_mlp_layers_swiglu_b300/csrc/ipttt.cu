@@ -28,7 +28,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 namespace {
 
 constexpr int kMaxTimedCalls = 256;
-constexpr int kBoundaries = IPTTT_NUM_STAGES + 1;
+// Timing events recorded per timed layer call.
+enum : int {
+  kEvStart = 0,       // context stream, before the fork
+  kEvConvStart = 1,   // side stream
+  kEvConvEnd = 2,     // side stream
+  kEvSwigluEnd = 3,   // context stream
+  kEvJoined = 4,      // context stream, after waiting for the conv
+  kEvTargetEnd = 5,
+  kEvStateEnd = 6,
+  kEvApplyEnd = 7,
+  kEventsPerCall = 8
+};
 
 }  // namespace
 
@@ -40,6 +51,10 @@ struct ipttt_ctx {
   uint64_t wait_limit_ns = 2000000000ull;
   EncodeTiledFn encode = nullptr;
   bool attrs_set = false;
+  // The causal conv runs on an internal side stream, forked from and joined back into
+  // `stream` with these events, so that it overlaps the SwiGLU GEMM.
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
   // timing
   bool timing = false;
   int timed_calls = 0;
@@ -446,8 +461,8 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
   return check_launch(ctx, "apply launch");
 }
 
-void mark(ipttt_ctx* ctx, int call, int boundary) {
-  if (call >= 0) cudaEventRecord(ctx->events[(size_t)call * kBoundaries + boundary], ctx->stream);
+void mark(ipttt_ctx* ctx, int call, int which, cudaStream_t stream) {
+  if (call >= 0) cudaEventRecord(ctx->events[(size_t)call * kEventsPerCall + which], stream);
 }
 
 // The layer on device buffers, validated by the caller.
@@ -475,18 +490,33 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   void* Wst = base + L.w;
   int call = -1;
   if (ctx->timing && ctx->timed_calls < kMaxTimedCalls) call = ctx->timed_calls++;
-  mark(ctx, call, 0);
+  cudaError_t e;
+  mark(ctx, call, kEvStart, ctx->stream);
+  // fork: the causal conv (memory bound) overlaps the SwiGLU GEMM (tensor bound)
+  if ((e = cudaEventRecord(ctx->fork, ctx->stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(ctx->side, ctx->fork, 0)) != cudaSuccess)
+    return cuda_fail(ctx, e, "fork");
+  {
+    cudaStream_t main_stream = ctx->stream;
+    ctx->stream = ctx->side;
+    mark(ctx, call, kEvConvStart, ctx->side);
+    s = run_conv(ctx, X0, cw, B, T, d, k, dt, Y);
+    mark(ctx, call, kEvConvEnd, ctx->side);
+    ctx->stream = main_stream;
+    if (s != IPTTT_OK) return s;
+  }
+  if ((e = cudaEventRecord(ctx->join, ctx->side)) != cudaSuccess) return cuda_fail(ctx, e, "join record");
   if ((s = run_swiglu(ctx, H, Wg, Wu, B * T, d, f, dt, Z)) != IPTTT_OK) return s;
-  mark(ctx, call, 1);
-  if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, Y)) != IPTTT_OK) return s;
-  mark(ctx, call, 2);
+  mark(ctx, call, kEvSwigluEnd, ctx->stream);
+  if ((e = cudaStreamWaitEvent(ctx->stream, ctx->join, 0)) != cudaSuccess) return cuda_fail(ctx, e, "join");
+  mark(ctx, call, kEvJoined, ctx->stream);
   if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V)) != IPTTT_OK) return s;
-  mark(ctx, call, 3);
+  mark(ctx, call, kEvTargetEnd, ctx->stream);
   const bool bf16 = dt == IPTTT_BF16;  // W_eff[b, 0] = W_down0: the apply reads W_down0 itself
   if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, bf16)) != IPTTT_OK) return s;
-  mark(ctx, call, 4);
+  mark(ctx, call, kEvStateEnd, ctx->stream);
   if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, bf16 ? W0 : nullptr)) != IPTTT_OK) return s;
-  mark(ctx, call, 5);
+  mark(ctx, call, kEvApplyEnd, ctx->stream);
   if (call >= 0) ctx->timed_launches += ipttt_layer_launches(B, T, dt);
   return IPTTT_OK;
 }
@@ -605,7 +635,13 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
     delete ctx;
     return IPTTT_ERR_CUDA;
   }
-  ctx->events.resize((size_t)kMaxTimedCalls * kBoundaries, nullptr);
+  if (cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->join, cudaEventDisableTiming) != cudaSuccess) {
+    ipttt_destroy(ctx);
+    return IPTTT_ERR_CUDA;
+  }
+  ctx->events.resize((size_t)kMaxTimedCalls * kEventsPerCall, nullptr);
   for (auto& e : ctx->events) {
     if (cudaEventCreate(&e) != cudaSuccess) {
       ipttt_destroy(ctx);
@@ -659,6 +695,9 @@ void ipttt_destroy(ipttt_ctx* ctx) {
   DeviceGuard g(ctx->device);
   for (auto& e : ctx->events)
     if (e) cudaEventDestroy(e);
+  if (ctx->fork) cudaEventDestroy(ctx->fork);
+  if (ctx->join) cudaEventDestroy(ctx->join);
+  if (ctx->side) cudaStreamDestroy(ctx->side);
   if (ctx->status) cudaFree(ctx->status);
   delete ctx;
 }
@@ -838,13 +877,21 @@ ipttt_status ipttt_timing_read(ipttt_ctx* ctx, double* ms, int64_t* calls, int64
   DeviceGuard g(ctx->device);
   ctx->timing = false;
   for (int s = 0; s < IPTTT_NUM_STAGES; ++s) ms[s] = 0.0;
+  // stage intervals: swiglu [start, swiglu end], conv [conv start, conv end] on the side stream
+  // (overlapping the SwiGLU GEMM), target [joined, target end], state, apply
+  const int iv[IPTTT_NUM_STAGES][2] = {{kEvStart, kEvSwigluEnd},
+                                       {kEvConvStart, kEvConvEnd},
+                                       {kEvJoined, kEvTargetEnd},
+                                       {kEvTargetEnd, kEvStateEnd},
+                                       {kEvStateEnd, kEvApplyEnd}};
   for (int c = 0; c < ctx->timed_calls; ++c) {
-    cudaEvent_t* ev = &ctx->events[(size_t)c * kBoundaries];
-    cudaError_t e = cudaEventSynchronize(ev[kBoundaries - 1]);
+    cudaEvent_t* ev = &ctx->events[(size_t)c * kEventsPerCall];
+    cudaError_t e = cudaEventSynchronize(ev[kEvApplyEnd]);
+    if (e == cudaSuccess) e = cudaEventSynchronize(ev[kEvConvEnd]);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "timing event");
     for (int s = 0; s < IPTTT_NUM_STAGES; ++s) {
       float t = 0.f;
-      e = cudaEventElapsedTime(&t, ev[s], ev[s + 1]);
+      e = cudaEventElapsedTime(&t, ev[iv[s][0]], ev[iv[s][1]]);
       if (e != cudaSuccess) return cuda_fail(ctx, e, "timing elapsed");
       ms[s] += t;
     }
