@@ -350,6 +350,15 @@ def finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks,
     peaks, peak_src = load_peaks()
     fl = stage_flops(w)
     by = stage_bytes(w)
+    stage_ms = dict(stage_ms)
+    if stage_ms.get("apply", 0.0) == 0.0:
+        # steps (3)-(5) ran as one fused kernel, timed as the "state" stage
+        es = 2 if w.dtype == "bf16" else 4
+        BT = w.B * w.T
+        stage_ms["state_apply"] = stage_ms.pop("state")
+        stage_ms.pop("apply")
+        fl["state_apply"] = fl["state"] + fl["apply"]
+        by["state_apply"] = es * (2 * BT * w.d + BT * w.d_ff + w.d * w.d_ff) + 4 * w.B * w.d * w.d_ff
     per_launch = {s: stage_ms[s] / timed_calls for s in stage_ms}
     kernels = {}
     for s, ms in per_launch.items():

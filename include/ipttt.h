@@ -66,8 +66,8 @@ typedef enum {
   IPTTT_STAGE_SWIGLU = 0, /* step (1)                                     */
   IPTTT_STAGE_CONV = 1,   /* causal conv of step (2), overlapping (1)     */
   IPTTT_STAGE_TARGET = 2, /* W_target projection of step (2), times eta   */
-  IPTTT_STAGE_STATE = 3,  /* steps (3)+(4): chunk updates and prefix      */
-  IPTTT_STAGE_APPLY = 4,  /* step (5)                                     */
+  IPTTT_STAGE_STATE = 3,  /* steps (3)+(4); with the fused kernel (3)-(5) */
+  IPTTT_STAGE_APPLY = 4,  /* step (5); 0 with the fused kernel            */
   IPTTT_NUM_STAGES = 5
 } ipttt_stage;
 
@@ -87,6 +87,13 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* cuda_stream);
 /* Rebind the context to another stream of the same device. */
 ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* cuda_stream);
 
+/* bf16 layer calls run steps (3)-(5) as one cooperative kernel by default: the state units
+ * run first and the per-chunk apply tiles fill the SMs the state work leaves idle (each tile
+ * waits on device-side counters until the weights of its chunk are written).  enable = 0
+ * selects two separate kernels instead (same results, bit for bit); devices without
+ * cooperative launch always use two. */
+ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable);
+
 /* Limit, in nanoseconds, on every device-side wait of later launches (default 2e9). */
 ipttt_status ipttt_set_wait_limit_ns(ipttt_ctx* ctx, uint64_t ns);
 
@@ -103,7 +110,7 @@ void ipttt_destroy(ipttt_ctx* ctx);
 
 /* Bytes of device workspace ipttt_layer_forward needs for this shape (host-only call, no
  * GPU needed).  Layout: Y [B,T,d], V [B,T,d], Z [B,T,d_ff], W stack [B,ceil(T/C),d,d_ff],
- * each in `dtype`, each region 256-byte aligned.
+ * each in `dtype`, then B*ceil(T/C)+1 uint32 counters; each region 256-byte aligned.
  * Errors: INVALID_ARG (bytes == NULL, negative sizes, C < 1, k < 1), UNSUPPORTED. */
 ipttt_status ipttt_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
                                   ipttt_dtype dtype, size_t* bytes);
@@ -221,7 +228,8 @@ ipttt_status ipttt_timing_begin(ipttt_ctx* ctx);
  * *calls and the number of kernels those calls launched to *launches. */
 ipttt_status ipttt_timing_read(ipttt_ctx* ctx, double* ms, int64_t* calls, int64_t* launches);
 
-/* Number of kernels one ipttt_layer_forward call launches for this shape (host only). */
+/* Number of kernels one ipttt_layer_forward call launches for this shape with the default
+ * settings (host only): bf16 4 (fused steps 3-5), fp32 6; T = 0: 1; B = 0: 0. */
 int64_t ipttt_layer_launches(int64_t B, int64_t T, ipttt_dtype dtype);
 
 /* Launch one block that waits on a shared-memory barrier nothing ever signals, through

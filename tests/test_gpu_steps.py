@@ -87,19 +87,23 @@ def test_chunk_apply_step(ctx, dt, B, T, d, f, C):
         assert rel_err(O[b], oracle.chunk_apply(Z[b], W_eff[b], C)) <= STEP_TOL[dt]
 
 
-def test_steps_compose_to_the_layer(ctx):
-    """The layer call equals its documented step sequence, bit for bit."""
+@pytest.mark.parametrize("fused", [True, False])
+def test_steps_compose_to_the_layer(ctx, fused):
+    """The layer call (fused state + apply kernel or two kernels) equals its documented step
+    sequence, bit for bit."""
     import weight_mlp_layers_swiglu_b300 as pkg
     from weight_mlp_layers_swiglu_b300.inputs import random_case
 
     w, x = random_case(2, 384, 256, 512, 128, 4, 1.0 / 128, "bf16", 21)
     xd = {k: v.cuda() for k, v in x.items()}
+    ctx.set_fused_tail(fused)
     O, Wf = ctx.layer_forward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
                               xd["conv_w"], w.C, w.eta)
+    ctx.set_fused_tail(True)
     Z = ctx.swiglu(xd["H"].view(-1, w.d), xd["W_gate"], xd["W_up"]).view(w.B, w.T, w.d_ff)
     V, _ = ctx.target(xd["X0"], xd["conv_w"], xd["W_target"], w.eta)
     W_eff, Wf2 = ctx.chunk_state(V, Z, xd["W_down0"], w.C)
     O2 = ctx.chunk_apply(Z, W_eff, w.C)
     assert ctx.sync() == 0
     assert torch.equal(O, O2) and torch.equal(Wf, Wf2)
-    assert pkg.layer_launches(w.B, w.T, pkg.BF16) == 5
+    assert pkg.layer_launches(w.B, w.T, pkg.BF16) == 4

@@ -16,6 +16,7 @@
 #include "../../include/ipttt.h"
 #include "ptx.cuh"
 #include "simt.cuh"
+#include "tc_fused.cuh"
 #include "tc_gemm.cuh"
 #include "tc_state.cuh"
 
@@ -51,6 +52,8 @@ struct ipttt_ctx {
   uint64_t wait_limit_ns = 2000000000ull;
   EncodeTiledFn encode = nullptr;
   bool attrs_set = false;
+  bool coop = false;       // device supports cooperative launches
+  bool fused_tail = true;  // run steps (3)-(5) as one cooperative kernel when possible
   // The causal conv runs on an internal side stream, forked from and joined back into
   // `stream` with these events, so that it overlaps the SwiGLU GEMM.
   cudaStream_t side = nullptr;
@@ -60,6 +63,7 @@ struct ipttt_ctx {
   int timed_calls = 0;
   int64_t timed_launches = 0;
   std::vector<cudaEvent_t> events;
+  std::vector<char> timed_fused;  // per timed call: steps (3)-(5) ran as one kernel
   std::string err;
 };
 
@@ -152,7 +156,7 @@ ipttt_status check_shape(ipttt_ctx* ctx, int64_t B, int64_t T, int64_t d, int64_
 int64_t n_chunks_of(int64_t T, int64_t C) { return T == 0 ? 0 : (T + C - 1) / C; }
 
 struct WsLayout {
-  size_t y, v, z, w, total;
+  size_t y, v, z, w, ctr, total;
 };
 
 WsLayout ws_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, ipttt_dtype dt) {
@@ -167,6 +171,8 @@ WsLayout ws_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, ipttt_
   off += align256((size_t)B * T * f * es);
   L.w = off;
   off += align256((size_t)B * n_chunks_of(T, C) * d * f * es);
+  L.ctr = off;  // hand-off counters of the fused state + apply kernel: B*n slices + queue head
+  off += align256(((size_t)B * n_chunks_of(T, C) + 1) * sizeof(uint32_t));
   L.total = off;
   return L;
 }
@@ -248,6 +254,9 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
   e = cudaFuncSetAttribute(state::tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            state::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (state)");
+  e = cudaFuncSetAttribute(fused::tc_state_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           fused::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (state+apply)");
   ctx->attrs_set = true;
   return IPTTT_OK;
 }
@@ -323,8 +332,10 @@ ipttt_status run_conv(ipttt_ctx* ctx, const void* X0, const void* cw, int64_t B,
   return check_launch(ctx, "conv launch");
 }
 
+// zero_ptr / zero_count (bf16 only): words the kernel clears before the fused state + apply
+// kernel that follows it on the stream uses them as counters.
 ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int64_t rows, int64_t d, float scale,
-                             ipttt_dtype dt, void* V) {
+                             ipttt_dtype dt, void* V, uint32_t* zero_ptr = nullptr, int zero_count = 0) {
   if (rows == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
     CUtensorMap ma, mb, mo;
@@ -338,6 +349,8 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
     p.problems = 1;
     p.group_m = 16;
     p.scale = scale;
+    p.zero_ptr = zero_ptr;
+    p.zero_count = zero_count;
     p.st = dev_status(ctx);
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
@@ -461,6 +474,59 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
   return check_launch(ctx, "apply launch");
 }
 
+// Steps (3)-(5) as one cooperative kernel: state unit pairs, then apply tiles from a queue
+// (tc_fused.cuh).  `ctr` holds B*n slice counters and the queue head, zeroed beforehand.
+ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
+                                   int64_t d, int64_t f, int64_t C, void* W_eff, float* W_final, void* O,
+                                   uint32_t* ctr) {
+  const int64_t n = n_chunks_of(T, C);
+  CUtensorMap mv, mz, mw_st, mf, mza, mw_ld, mw0, mo;
+  if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64) ||
+      !map_3d(ctx, &mw_st, W_eff, B * n, d, f, 32) || !map_3d_f32(ctx, &mf, W_final, B, d, f, 32) ||
+      !map_3d(ctx, &mza, Z, B, T, f, 128) || !map_3d(ctx, &mw_ld, W_eff, B * n, d, f, 256) ||
+      !map_2d(ctx, &mw0, W0, d, f, 64, 256) || !map_3d(ctx, &mo, O, B, T, d, 32))
+    return IPTTT_ERR_CUDA;
+  fused::Params p{};
+  p.s.B = (int)B;
+  p.s.T = (int)T;
+  p.s.d = (int)d;
+  p.s.f = (int)f;
+  p.s.C = (int)C;
+  p.s.n_chunks = (int)n;
+  p.s.m_units = ceil_div(d, state::BMD);
+  p.s.n_units = ceil_div(f, state::BNF);
+  p.s.units = (int)(B * p.s.m_units * p.s.n_units);
+  p.s.W0 = static_cast<const __nv_bfloat16*>(W0);
+  p.s.skip_first = 1;
+  p.s.st = dev_status(ctx);
+  p.a.m_tiles = (int)(C / gemm::BM);
+  p.a.n_tiles = ceil_div(d, gemm::BN);
+  p.a.k_blocks = ceil_div(f, gemm::BK);
+  p.a.problems = (int)(B * n);
+  p.a.group_m = 16;
+  p.a.scale = 1.f;
+  p.a.T = (int)T, p.a.C = (int)C, p.a.n_chunks = (int)n;
+  p.a.first_from_w0 = 1;
+  p.a.st = dev_status(ctx);
+  p.ready = ctr;
+  p.next_tile = ctr + B * n;
+  p.ready_target = (uint32_t)(p.s.m_units * p.s.n_units * 4);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctx->sm_count);
+  cfg.blockDim = dim3(fused::NUM_THREADS);
+  cfg.dynamicSmemBytes = fused::SMEM_BYTES;
+  cfg.stream = ctx->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, fused::tc_state_apply_kernel, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "state+apply launch");
+  return check_launch(ctx, "state+apply launch");
+}
+
 void mark(ipttt_ctx* ctx, int call, int which, cudaStream_t stream) {
   if (call >= 0) cudaEventRecord(ctx->events[(size_t)call * kEventsPerCall + which], stream);
 }
@@ -489,7 +555,10 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   void* Z = base + L.z;
   void* Wst = base + L.w;
   int call = -1;
-  if (ctx->timing && ctx->timed_calls < kMaxTimedCalls) call = ctx->timed_calls++;
+  if (ctx->timing && ctx->timed_calls < kMaxTimedCalls) {
+    call = ctx->timed_calls++;
+    ctx->timed_fused[call] = 0;
+  }
   cudaError_t e;
   mark(ctx, call, kEvStart, ctx->stream);
   // fork: the causal conv (memory bound) overlaps the SwiGLU GEMM (tensor bound)
@@ -510,14 +579,25 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   mark(ctx, call, kEvSwigluEnd, ctx->stream);
   if ((e = cudaStreamWaitEvent(ctx->stream, ctx->join, 0)) != cudaSuccess) return cuda_fail(ctx, e, "join");
   mark(ctx, call, kEvJoined, ctx->stream);
-  if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V)) != IPTTT_OK) return s;
-  mark(ctx, call, kEvTargetEnd, ctx->stream);
   const bool bf16 = dt == IPTTT_BF16;  // W_eff[b, 0] = W_down0: the apply reads W_down0 itself
-  if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, bf16)) != IPTTT_OK) return s;
-  mark(ctx, call, kEvStateEnd, ctx->stream);
-  if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, bf16 ? W0 : nullptr)) != IPTTT_OK) return s;
-  mark(ctx, call, kEvApplyEnd, ctx->stream);
-  if (call >= 0) ctx->timed_launches += ipttt_layer_launches(B, T, dt);
+  const bool fuse = bf16 && ctx->fused_tail && ctx->coop;
+  uint32_t* ctr = reinterpret_cast<uint32_t*>(base + L.ctr);
+  const int n_ctr = (int)(B * n_chunks_of(T, C) + 1);
+  if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V, fuse ? ctr : nullptr, fuse ? n_ctr : 0)) != IPTTT_OK)
+    return s;
+  mark(ctx, call, kEvTargetEnd, ctx->stream);
+  if (fuse) {
+    if ((s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr)) != IPTTT_OK) return s;
+    mark(ctx, call, kEvStateEnd, ctx->stream);
+    mark(ctx, call, kEvApplyEnd, ctx->stream);
+    if (call >= 0) ctx->timed_fused[call] = 1;
+  } else {
+    if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, bf16)) != IPTTT_OK) return s;
+    mark(ctx, call, kEvStateEnd, ctx->stream);
+    if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, bf16 ? W0 : nullptr)) != IPTTT_OK) return s;
+    mark(ctx, call, kEvApplyEnd, ctx->stream);
+  }
+  if (call >= 0) ctx->timed_launches += bf16 ? (fuse ? 4 : 5) : 6;
   return IPTTT_OK;
 }
 
@@ -618,6 +698,7 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
     return IPTTT_ERR_CUDA;
   }
   ctx->sm_count = prop.multiProcessorCount;
+  ctx->coop = prop.cooperativeLaunch != 0;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -642,6 +723,7 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
     return IPTTT_ERR_CUDA;
   }
   ctx->events.resize((size_t)kMaxTimedCalls * kEventsPerCall, nullptr);
+  ctx->timed_fused.assign(kMaxTimedCalls, 0);
   for (auto& e : ctx->events) {
     if (cudaEventCreate(&e) != cudaSuccess) {
       ipttt_destroy(ctx);
@@ -655,6 +737,12 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
 ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* stream) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
   ctx->stream = static_cast<cudaStream_t>(stream);
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ctx->fused_tail = enable != 0;
   return IPTTT_OK;
 }
 
@@ -725,7 +813,7 @@ ipttt_status ipttt_host_workspace_size(int64_t B, int64_t T, int64_t d, int64_t 
 int64_t ipttt_layer_launches(int64_t B, int64_t T, ipttt_dtype dt) {
   if (B <= 0) return 0;
   if (T <= 0) return 1;
-  return dt == IPTTT_BF16 ? 5 : 6;
+  return dt == IPTTT_BF16 ? 4 : 6;
 }
 
 ipttt_status ipttt_layer_forward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate, const void* W_up,
@@ -891,6 +979,7 @@ ipttt_status ipttt_timing_read(ipttt_ctx* ctx, double* ms, int64_t* calls, int64
     if (e != cudaSuccess) return cuda_fail(ctx, e, "timing event");
     for (int s = 0; s < IPTTT_NUM_STAGES; ++s) {
       float t = 0.f;
+      if (s == IPTTT_STAGE_APPLY && ctx->timed_fused[c]) continue;  // included in the state stage
       e = cudaEventElapsedTime(&t, ev[iv[s][0]], ev[iv[s][1]]);
       if (e != cudaSuccess) return cuda_fail(ctx, e, "timing elapsed");
       ms[s] += t;

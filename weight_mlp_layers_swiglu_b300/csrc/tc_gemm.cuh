@@ -50,6 +50,8 @@ struct Params {
   float scale;
   int T, C, n_chunks;  // Apply only
   int first_from_w0;   // Apply: chunk 0 of each sequence reads W_down0 (map_b1) instead of the stack
+  uint32_t* zero_ptr;  // optional: CTA 0 clears zero_count words here (counters of a later kernel)
+  int zero_count;
   DevStatus st;
 };
 
@@ -94,6 +96,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int total_tiles = p.problems * p.m_tiles * p.n_tiles;
+
+  if (p.zero_ptr != nullptr && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.zero_count; i += blockDim.x) p.zero_ptr[i] = 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {

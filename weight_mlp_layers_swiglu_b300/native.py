@@ -31,6 +31,7 @@ _SIGNATURES = {
     "ipttt_create": (ctypes.c_int, [ctypes.POINTER(c_vp), ctypes.c_int, c_vp]),
     "ipttt_set_stream": (ctypes.c_int, [c_vp, c_vp]),
     "ipttt_set_wait_limit_ns": (ctypes.c_int, [c_vp, ctypes.c_uint64]),
+    "ipttt_set_fused_tail": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_sync": (ctypes.c_int, [c_vp]),
     "ipttt_last_error": (ctypes.c_char_p, [c_vp]),
     "ipttt_destroy": (None, [c_vp]),
@@ -157,6 +158,9 @@ class Context:
     def set_stream(self, stream: torch.cuda.Stream):
         self.stream = stream
         self._check(self.lib.ipttt_set_stream(self.h, c_vp(stream.cuda_stream)), "set_stream")
+
+    def set_fused_tail(self, enable: bool):
+        self._check(self.lib.ipttt_set_fused_tail(self.h, 1 if enable else 0), "set_fused_tail")
 
     def set_wait_limit_ns(self, ns: int):
         self._check(self.lib.ipttt_set_wait_limit_ns(self.h, int(ns)), "set_wait_limit_ns")
