@@ -9,6 +9,10 @@ d_ff=9728, C=1024, k=4, eta=1/1024, bf16).  Inputs are seeded synthetic tensors,
 in HBM before the timed region; the per-step working set (~0.5 GB of inputs, ~2.6 GB of
 workspace) is larger than the 126 MB L2, so no flush is needed between steps.
 
+The line also carries a streaming leg: the same sequence fed as consecutive calls of
+--stream-tokens tokens (default 1024, one chunk), each resuming from the previous call's
+fast-weight state and conv halo.
+
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own sequence of
 the workload (independent fast-weight states, no collective on the data path): weak scaling.
 
@@ -298,10 +302,46 @@ def run_ours(args, w):
     ms_max = max_over_ranks(ms_total, world, dev)
 
     e2e = None if args.no_e2e else e2e_leg(args, w, ctx, weights, H_host, X_host, dev, world)
+    stream = stream_leg(args, w, ctx, weights, H, X0, dev, world) if args.stream_tokens else None
     if rank != 0:
         return 0
-    finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks, e2e, H)
+    finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks, e2e, H, stream)
     return 0
+
+
+def stream_leg(args, w, ctx, weights, H, X0, dev, world):
+    """The same sequence fed as consecutive calls of `stream_tokens` tokens, each continuing
+    from the previous call's fast-weight state and conv halo (the streaming / decode use)."""
+    import torch
+
+    import weight_mlp_layers_swiglu_b300 as pkg
+
+    S = args.stream_tokens
+    cuts = list(range(0, w.T, S))
+    Hs = [H[:, lo:lo + S].contiguous() for lo in cuts]
+    Xs = [X0[:, lo:lo + S].contiguous() for lo in cuts]
+    stream = torch.cuda.current_stream(dev)
+
+    def one_pass():
+        sl = pkg.StreamingLayer(ctx, weights["W_gate"], weights["W_up"], weights["W_down0"], weights["W_target"],
+                                weights["conv_w"], w.B, w.C, w.eta)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for h, x in zip(Hs, Xs):
+            sl.step(h, x)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    one_pass()
+    passes = 5
+    ms = sum(one_pass() for _ in range(passes)) / passes
+    if ctx.sync() != 0:
+        raise RuntimeError(f"device status in the streaming leg: {ctx.last_error()}")
+    ms = max_over_ranks(ms, world, dev)
+    return {"call_tokens": S, "calls_per_sequence": len(cuts), "value": w.B * w.T * world / (ms * 1e-3),
+            "unit": UNIT, "ms_per_sequence": ms}
 
 
 def e2e_leg(args, w, ctx, weights, H_host, X_host, dev, world):
@@ -344,7 +384,7 @@ def e2e_leg(args, w, ctx, weights, H_host, X_host, dev, world):
             "d2h_bytes_per_step": d2h}
 
 
-def finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks, e2e, H):
+def finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks, e2e, H, stream=None):
     import weight_mlp_layers_swiglu_b300 as pkg
 
     peaks, peak_src = load_peaks()
@@ -386,6 +426,8 @@ def finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks,
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches * world if timed_calls == args.steps
             else pkg.layer_launches(w.B, w.T, pkg.dtype_code(H.dtype)) * args.steps * world,
             "e2e": e2e, "clocks": clocks.summary()}
+    if stream is not None:
+        line["stream"] = stream
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = oracle_sample(w, seconds=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -432,6 +474,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--stream-tokens", type=int, default=1024,
+                    help="tokens per call of the streaming leg (0 = skip it)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (a shorter case of the same shapes, e.g. for profiler captures)")
     args = ap.parse_args(argv)

@@ -133,6 +133,30 @@ ipttt_status ipttt_layer_forward(ipttt_ctx* ctx, const void* H, const void* X0, 
                                  int64_t C, int k, float eta, ipttt_dtype dtype, void* O,
                                  float* W_final, void* workspace, size_t workspace_bytes);
 
+/* Continue B sequences where an earlier call left them: streaming, read-while-learn use
+ * (zhichai.net page §9, future directions; one fast-weight state per session as in the
+ * travelaiplan.net engineering blog §4).  Same computation as ipttt_layer_forward, except that
+ *   W_state     [B, d, d_ff]  fp32, device   each sequence's fast weight at this call's first
+ *                                            token (W_down0 broadcast for a new sequence; the
+ *                                            W_state_out of the previous call otherwise)
+ *   X0_halo     [B, k-1, d]   dtype, device  the k-1 X0 rows before this call's first token
+ *                                            (NULL = zeros: a new sequence)
+ *   W_state_out [B, d, d_ff]  fp32, device   the state after this call's last chunk; may be
+ *                                            W_state itself (updated in place)
+ *   X0_halo_out [B, k-1, d]   dtype, device  (NULL = not written) the last k-1 rows of
+ *                                            [X0_halo, X0], the next call's X0_halo; must not
+ *                                            overlap X0_halo
+ * Chunks are counted from this call's first token, so a sequence cut at multiples of C and
+ * fed call by call gives exactly the results of one call over the whole sequence (bit for bit
+ * on the GPU).  A call of T = C tokens is the decode step: buffer C tokens, then run them.
+ * The workspace is that of ipttt_layer_forward.  Errors as ipttt_layer_forward. */
+ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                        const void* W_up, const void* W_target, const void* conv_w,
+                                        const float* W_state, const void* X0_halo, int64_t B, int64_t T,
+                                        int64_t d, int64_t d_ff, int64_t C, int k, float eta,
+                                        ipttt_dtype dtype, void* O, float* W_state_out, void* X0_halo_out,
+                                        void* workspace, size_t workspace_bytes);
+
 /* Bytes of device workspace ipttt_layer_forward_host needs: ipttt_workspace_size() plus
  * device staging for H, X0, O and W_final. */
 ipttt_status ipttt_host_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,

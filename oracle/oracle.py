@@ -39,6 +39,7 @@ design notes of the repository):
     own fast-weight state; the frozen weights are shared.
 
 Parity status: every function here is pinned by tests in tests/test_oracle_pins.py
+and tests/test_oracle_stream.py
 (hand-derived worked examples, closed forms, library routines, invariants and an
 independent plain-C twin).  No function is "parity unpinned".
 """
@@ -71,26 +72,27 @@ def swiglu(H, W_gate, W_up) -> np.ndarray:
     return silu(H @ W_gate.T) * (H @ W_up.T)
 
 
-def causal_conv(X0, conv_w) -> np.ndarray:
+def causal_conv(X0, conv_w, halo=None) -> np.ndarray:
     """Y = causal depthwise Conv1D(X0)  ([zhichai] §3.3, target equation, "causal padding").
 
-    X0: [T, d]; conv_w: [d, k].  Y[t, c] = sum_s conv_w[c, s] * X0[t - (k-1) + s, c],
-    terms with a negative token index are zero (left padding of k-1).
+    X0: [T, d]; conv_w: [d, k].  Y[t, c] = sum_s conv_w[c, s] * X0[t - (k-1) + s, c].
+    Token indices before 0 read `halo` ([k-1, d], the k-1 tokens that precede X0 when a
+    sequence is processed in several calls) or are zero (left padding of k-1) without one.
     """
     X0, conv_w = _f64(X0), _f64(conv_w)
     T, d = X0.shape
     k = conv_w.shape[1]
+    pad = np.zeros((k - 1, d)) if halo is None else _f64(halo).reshape(k - 1, d)
+    Xp = np.concatenate([pad, X0])  # Xp[t + k - 1] = X0[t]
     Y = np.zeros((T, d))
     for s in range(k):
-        back = (k - 1) - s  # tap s reads the token `back` steps before t
-        if back < T:
-            Y[back:] += conv_w[:, s] * X0[: T - back]
+        Y += conv_w[:, s] * Xp[s: s + T]
     return Y
 
 
-def target(X0, conv_w, W_target) -> np.ndarray:
+def target(X0, conv_w, W_target, halo=None) -> np.ndarray:
     """V = Conv1D(X0) W_target  ([zhichai] §3.3, LM-aligned target).  Returns [T, d]."""
-    return causal_conv(X0, conv_w) @ _f64(W_target)
+    return causal_conv(X0, conv_w, halo) @ _f64(W_target)
 
 
 def chunk_delta(V, Z) -> np.ndarray:
@@ -107,17 +109,18 @@ def chunk_rows(T: int, C: int):
     return [(s, min(s + C, T)) for s in range(0, T, C)]
 
 
-def sequence_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float):
+def sequence_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, halo=None):
     """One sequence, the literal sequential chunk loop.
 
     For each chunk in order: the chunk's output is computed with the current
     fast weight, then the fast weight takes one step
     W <- W + eta * V_i^T Z_i  ([zhichai] §3.2 bullets and §3.3 update rule;
     [xiaoxiang] "核心方法" item 3: output first with the previous weight, then update).
-    Returns O [T, d] and the final W_down [d, d_ff].
+    W_down0 is the fast weight at the first token ([d, d_ff]); `halo` the k-1 X0 rows
+    before it (see causal_conv).  Returns O [T, d] and the final W_down [d, d_ff].
     """
     Z = swiglu(H, W_gate, W_up)
-    V = target(X0, conv_w, W_target)
+    V = target(X0, conv_w, W_target, halo)
     W = _f64(W_down0).copy()
     T = Z.shape[0]
     O = np.zeros((T, W.shape[0]))
@@ -143,6 +146,33 @@ def layer_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: f
     for b in range(B):
         O[b], Wf[b] = sequence_forward(H[b], X0[b], W_gate, W_up, W_down0, W_target, conv_w, C, eta)
     return O, Wf
+
+
+def layer_resume(H, X0, W_gate, W_up, W_target, conv_w, W_state, X0_halo, C: int, eta: float):
+    """Continue every sequence of a batch from where an earlier call left it.
+
+    The fast weight is carried from call to call: the pages' stated direction is read-while-
+    learn streaming inference with one fast-weight state per session ([zhichai] §9 future
+    directions; [travelaiplan] §4).  W_state [B, d, d_ff] is each sequence's fast weight at its
+    first token of this call; X0_halo [B, k-1, d] its k-1 preceding X0 rows (zeros at the start
+    of a sequence).  Chunks are counted from this call's first token, so a sequence split at a
+    multiple of C gives the same result as one call over the whole sequence.
+    Returns O [B, T, d], the final state [B, d, d_ff] and the new halo [B, k-1, d] (the last
+    k-1 rows of [X0_halo, X0]).
+    """
+    H, X0 = _f64(H), _f64(X0)
+    W_state, X0_halo = _f64(W_state), _f64(X0_halo)
+    B, T, d = H.shape
+    k = _f64(conv_w).shape[1]
+    f = _f64(W_gate).shape[0]
+    O = np.zeros((B, T, d))
+    Wf = np.zeros((B, d, f))
+    halo_out = np.zeros((B, k - 1, d))
+    for b in range(B):
+        O[b], Wf[b] = sequence_forward(H[b], X0[b], W_gate, W_up, W_state[b], W_target, conv_w, C, eta,
+                                       halo=X0_halo[b])
+        halo_out[b] = np.concatenate([X0_halo[b], X0[b]])[T:]
+    return O, Wf, halo_out
 
 
 def chunk_weights(V, Z, W_down0, C: int, eta: float):

@@ -4,8 +4,8 @@ The compute lives in libipttt.so (hand-written tcgen05/TMA kernels, C ABI in
 include/ipttt.h); this package is its thin ctypes binding plus the seeded
 synthetic workloads.  There is no CPU fallback.
 """
-from .native import (BF16, F32, STAGES, Context, IptttError, dtype_code, exported_symbols, layer_launches, load,
-                     workspace_size)
+from .native import (BF16, F32, STAGES, Context, IptttError, StreamingLayer, dtype_code, exported_symbols,
+                     layer_launches, load, workspace_size)
 
-__all__ = ["BF16", "F32", "STAGES", "Context", "IptttError", "dtype_code", "exported_symbols", "layer_launches",
-           "load", "workspace_size"]
+__all__ = ["BF16", "F32", "STAGES", "Context", "IptttError", "StreamingLayer", "dtype_code", "exported_symbols",
+           "layer_launches", "load", "workspace_size"]

@@ -306,13 +306,14 @@ ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const voi
 
 template <typename E>
 void launch_conv(ipttt_ctx* ctx, dim3 grid, dim3 block, const void* X0, const void* cw, void* Y, int T_len, int d,
-                 int k) {
+                 int k, const void* halo) {
   const E* x = static_cast<const E*>(X0);
   const E* w = static_cast<const E*>(cw);
   E* y = static_cast<E*>(Y);
+  const E* h = static_cast<const E*>(halo);
   switch (k) {
 #define IPTTT_CONV_CASE(KK) \
-  case KK: simt::causal_conv_kernel<E, KK><<<grid, block, 0, ctx->stream>>>(x, w, y, T_len, d); break;
+  case KK: simt::causal_conv_kernel<E, KK><<<grid, block, 0, ctx->stream>>>(x, w, y, T_len, d, h); break;
     IPTTT_CONV_CASE(1) IPTTT_CONV_CASE(2) IPTTT_CONV_CASE(3) IPTTT_CONV_CASE(4)
     IPTTT_CONV_CASE(5) IPTTT_CONV_CASE(6) IPTTT_CONV_CASE(7) IPTTT_CONV_CASE(8)
 #undef IPTTT_CONV_CASE
@@ -321,14 +322,14 @@ void launch_conv(ipttt_ctx* ctx, dim3 grid, dim3 block, const void* X0, const vo
 }
 
 ipttt_status run_conv(ipttt_ctx* ctx, const void* X0, const void* cw, int64_t B, int64_t T, int64_t d, int k,
-                      ipttt_dtype dt, void* Y) {
+                      ipttt_dtype dt, void* Y, const void* halo = nullptr) {
   if (B == 0 || T == 0) return IPTTT_OK;
   dim3 block(32, 4);
   dim3 grid(ceil_div(d / 8, 32), ceil_div(T, (int64_t)simt::CONV_TS * 4), (unsigned)B);
   if (dt == IPTTT_BF16)
-    launch_conv<__nv_bfloat16>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k);
+    launch_conv<__nv_bfloat16>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k, halo);
   else
-    launch_conv<float>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k);
+    launch_conv<float>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k, halo);
   return check_launch(ctx, "conv launch");
 }
 
@@ -374,9 +375,10 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
 // Steps (3)+(4).  fp32: Step 1 (all Delta_i) then Step 2 (scan); bf16: one fused kernel.
 // skip_first (bf16): leave W_eff[b, 0] (= W_down0) unwritten; the layer's apply then reads
 // W_down0 for chunk 0 directly.
+// W_init (optional, [B, d, f] fp32): each sequence's own starting state instead of W0.
 ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
                        int64_t d, int64_t f, int64_t C, ipttt_dtype dt, void* W_eff, float* W_final,
-                       bool skip_first = false) {
+                       bool skip_first = false, const float* W_init = nullptr) {
   const int64_t n = n_chunks_of(T, C);
   if (B == 0 || n == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
@@ -395,7 +397,8 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
     p.n_units = ceil_div(f, state::BNF);
     p.units = (int)(B * p.m_units * p.n_units);
     p.W0 = static_cast<const __nv_bfloat16*>(W0);
-    p.skip_first = skip_first ? 1 : 0;
+    p.skip_first = (skip_first && W_init == nullptr) ? 1 : 0;
+    p.W_init = W_init;
     p.st = dev_status(ctx);
     const int pairs = (p.units + 1) / 2;
     const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
@@ -422,7 +425,7 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
   const int64_t df = d * f;
   dim3 g2(ceil_div(df, 256), (unsigned)B);
   simt::chunk_scan_f32_kernel<<<g2, 256, 0, ctx->stream>>>(static_cast<float*>(W_eff), static_cast<const float*>(W0),
-                                                             W_final, (int)B, (int)n, df);
+                                                             W_final, (int)B, (int)n, df, W_init);
   return check_launch(ctx, "scan launch");
 }
 
@@ -478,14 +481,19 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
 // (tc_fused.cuh).  `ctr` holds B*n slice counters and the queue head, zeroed beforehand.
 ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
                                    int64_t d, int64_t f, int64_t C, void* W_eff, float* W_final, void* O,
-                                   uint32_t* ctr) {
+                                   uint32_t* ctr, const float* W_init = nullptr) {
   const int64_t n = n_chunks_of(T, C);
   CUtensorMap mv, mz, mw_st, mf, mza, mw_ld, mw0, mo;
   if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64) ||
       !map_3d(ctx, &mw_st, W_eff, B * n, d, f, 32) || !map_3d_f32(ctx, &mf, W_final, B, d, f, 32) ||
       !map_3d(ctx, &mza, Z, B, T, f, 128) || !map_3d(ctx, &mw_ld, W_eff, B * n, d, f, 256) ||
-      !map_2d(ctx, &mw0, W0, d, f, 64, 256) || !map_3d(ctx, &mo, O, B, T, d, 32))
+      !map_3d(ctx, &mo, O, B, T, d, 32))
     return IPTTT_ERR_CUDA;
+  if (W_init == nullptr) {
+    if (!map_2d(ctx, &mw0, W0, d, f, 64, 256)) return IPTTT_ERR_CUDA;
+  } else {
+    mw0 = mw_ld;  // unused: chunk 0 reads W_eff[b, 0]
+  }
   fused::Params p{};
   p.s.B = (int)B;
   p.s.T = (int)T;
@@ -497,7 +505,8 @@ ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z,
   p.s.n_units = ceil_div(f, state::BNF);
   p.s.units = (int)(B * p.s.m_units * p.s.n_units);
   p.s.W0 = static_cast<const __nv_bfloat16*>(W0);
-  p.s.skip_first = 1;
+  p.s.skip_first = W_init == nullptr ? 1 : 0;
+  p.s.W_init = W_init;
   p.s.st = dev_status(ctx);
   p.a.m_tiles = (int)(C / gemm::BM);
   p.a.n_tiles = ceil_div(d, gemm::BN);
@@ -506,7 +515,7 @@ ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z,
   p.a.group_m = 16;
   p.a.scale = 1.f;
   p.a.T = (int)T, p.a.C = (int)C, p.a.n_chunks = (int)n;
-  p.a.first_from_w0 = 1;
+  p.a.first_from_w0 = p.s.skip_first;
   p.a.st = dev_status(ctx);
   p.ready = ctr;
   p.next_tile = ctr + B * n;
@@ -532,10 +541,33 @@ void mark(ipttt_ctx* ctx, int call, int which, cudaStream_t stream) {
 }
 
 // The layer on device buffers, validated by the caller.
+// W_init (optional, fp32 [B, d, f]): per-sequence starting state instead of W0; halo_in /
+// halo_out (optional, [B, k-1, d]): the X0 rows before this call / after it (resumed calls).
 ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
                        const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d, int64_t f,
-                       int64_t C, int k, float eta, ipttt_dtype dt, void* O, float* W_final, void* ws) {
+                       int64_t C, int k, float eta, ipttt_dtype dt, void* O, float* W_final, void* ws,
+                       const float* W_init = nullptr, const void* halo_in = nullptr, void* halo_out = nullptr) {
   if (B == 0) return IPTTT_OK;
+  if (halo_out != nullptr && k > 1) {
+    const int64_t nh = B * (k - 1) * d;
+    dim3 g(ceil_div(nh, 256));
+    if (dt == IPTTT_BF16)
+      simt::halo_out_kernel<__nv_bfloat16><<<g, 256, 0, ctx->stream>>>(
+          static_cast<const __nv_bfloat16*>(X0), static_cast<const __nv_bfloat16*>(halo_in),
+          static_cast<__nv_bfloat16*>(halo_out), (int)B, (int)T, (int)d, k - 1);
+    else
+      simt::halo_out_kernel<float><<<g, 256, 0, ctx->stream>>>(static_cast<const float*>(X0),
+                                                               static_cast<const float*>(halo_in),
+                                                               static_cast<float*>(halo_out), (int)B, (int)T,
+                                                               (int)d, k - 1);
+    ipttt_status hs = check_launch(ctx, "halo launch");
+    if (hs != IPTTT_OK) return hs;
+  }
+  if (T == 0 && W_init != nullptr) {
+    const cudaError_t e = cudaMemcpyAsync(W_final, W_init, (size_t)B * d * f * sizeof(float),
+                                          cudaMemcpyDeviceToDevice, ctx->stream);
+    return e == cudaSuccess ? IPTTT_OK : cuda_fail(ctx, e, "state copy");
+  }
   if (T == 0) {
     const int64_t df = d * f;
     dim3 g(ceil_div(df, 256), (unsigned)B);
@@ -569,7 +601,7 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
     cudaStream_t main_stream = ctx->stream;
     ctx->stream = ctx->side;
     mark(ctx, call, kEvConvStart, ctx->side);
-    s = run_conv(ctx, X0, cw, B, T, d, k, dt, Y);
+    s = run_conv(ctx, X0, cw, B, T, d, k, dt, Y, halo_in);
     mark(ctx, call, kEvConvEnd, ctx->side);
     ctx->stream = main_stream;
     if (s != IPTTT_OK) return s;
@@ -587,17 +619,19 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
     return s;
   mark(ctx, call, kEvTargetEnd, ctx->stream);
   if (fuse) {
-    if ((s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr)) != IPTTT_OK) return s;
+    if ((s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr, W_init)) != IPTTT_OK)
+      return s;
     mark(ctx, call, kEvStateEnd, ctx->stream);
     mark(ctx, call, kEvApplyEnd, ctx->stream);
     if (call >= 0) ctx->timed_fused[call] = 1;
   } else {
-    if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, bf16)) != IPTTT_OK) return s;
+    if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, bf16, W_init)) != IPTTT_OK) return s;
     mark(ctx, call, kEvStateEnd, ctx->stream);
-    if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, bf16 ? W0 : nullptr)) != IPTTT_OK) return s;
+    const void* w0_first = (bf16 && W_init == nullptr) ? W0 : nullptr;
+    if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, w0_first)) != IPTTT_OK) return s;
     mark(ctx, call, kEvApplyEnd, ctx->stream);
   }
-  if (call >= 0) ctx->timed_launches += bf16 ? (fuse ? 4 : 5) : 6;
+  if (call >= 0) ctx->timed_launches += (bf16 ? (fuse ? 4 : 5) : 6) + ((halo_out != nullptr && k > 1) ? 1 : 0);
   return IPTTT_OK;
 }
 
@@ -826,6 +860,55 @@ ipttt_status ipttt_layer_forward(ipttt_ctx* ctx, const void* H, const void* X0, 
   if (s != IPTTT_OK) return s;
   DeviceGuard g(ctx->device);
   return run_layer(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, O, W_final, ws);
+}
+
+ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                        const void* W_up, const void* W_target, const void* conv_w,
+                                        const float* W_state, const void* X0_halo, int64_t B, int64_t T, int64_t d,
+                                        int64_t d_ff, int64_t C, int k, float eta, ipttt_dtype dt, void* O,
+                                        float* W_state_out, void* X0_halo_out, void* ws, size_t ws_bytes) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  // the shared-weight checks of the plain layer, with W_state standing in for W_down0
+  ipttt_status s = validate_layer(ctx, H, X0, W_gate, W_up, W_state, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt,
+                                  O, W_state_out, ws, ws_bytes, false);
+  if (s != IPTTT_OK) return s;
+  if (B == 0) return IPTTT_OK;
+  if ((X0_halo && !aligned16(X0_halo)) || (X0_halo_out && !aligned16(X0_halo_out))) {
+    set_err(ctx, "halo buffer is not 16-byte aligned");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  const size_t es = esize(dt);
+  const size_t act = (size_t)B * T * d * es, wdf = (size_t)d * d_ff * es, state = (size_t)B * d * d_ff * 4;
+  const size_t halo = (size_t)B * (k - 1) * d * es;
+  const WsLayout L = ws_layout(B, T, d, d_ff, C, dt);
+  std::vector<Region> all = {{H, act, "H"},
+                             {X0, act, "X0"},
+                             {W_gate, wdf, "W_gate"},
+                             {W_up, wdf, "W_up"},
+                             {W_target, (size_t)d * d * es, "W_target"},
+                             {conv_w, (size_t)d * k * es, "conv_w"},
+                             {X0_halo, halo, "X0_halo"},
+                             {O, act, "O"},
+                             {X0_halo_out, halo, "X0_halo_out"},
+                             {ws, T > 0 ? L.total : 0, "workspace"}};
+  std::vector<Region> outs = {all[7], all[8], all[9]};
+  std::string what;
+  if (find_overlap(outs, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  // W_state_out may be W_state itself (each state element is read before it is rewritten), but
+  // must not partly overlap it or touch any other buffer
+  all.push_back({W_state, state, "W_state"});
+  std::vector<Region> st_out = {{W_state_out, state, "W_state_out"}};
+  if (W_state_out == W_state) all.pop_back();
+  if (find_overlap(st_out, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  return run_layer(ctx, H, X0, W_gate, W_up, nullptr, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, O,
+                   W_state_out, ws, W_state, X0_halo, X0_halo_out);
 }
 
 ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const void* X0_host, const void* W_gate,

@@ -52,9 +52,11 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const fl
   *reinterpret_cast<uint4*>(p) = w;
 }
 
+// halo (optional, [B, K-1, d]): the K-1 rows that precede X0's first token of each sequence
+// (rows of an earlier call); without it those rows are zero.
 template <typename T, int K>
 __global__ void causal_conv_kernel(const T* __restrict__ X0, const T* __restrict__ conv_w, T* __restrict__ Y,
-                                   int T_len, int d) {
+                                   int T_len, int d, const T* __restrict__ halo) {
   const int cg = blockIdx.x * blockDim.x + threadIdx.x;  // channel group of 8
   const int c0 = cg * 8;
   const int t0 = (blockIdx.y * blockDim.y + threadIdx.y) * CONV_TS;
@@ -74,6 +76,8 @@ __global__ void causal_conv_kernel(const T* __restrict__ X0, const T* __restrict
     const int src = t0 - (K - 1) + s;
     if (src >= 0) {
       load8<T>(xb + (int64_t)src * d, win[s]);
+    } else if (halo != nullptr) {
+      load8<T>(halo + ((int64_t)b * (K - 1) + (K - 1) + src) * d + c0, win[s]);
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e) win[s][e] = 0.f;
@@ -96,6 +100,26 @@ __global__ void causal_conv_kernel(const T* __restrict__ X0, const T* __restrict
 #pragma unroll
       for (int e = 0; e < 8; ++e) win[s][e] = win[s + 1][e];
   }
+}
+
+// halo_out[b, j] = row T-(k-1)+j of [halo_in[b], X0[b]] (the k-1 rows the next call of the
+// sequence needs); rows before the sequence start are halo_in rows or zero.
+template <typename T>
+__global__ void halo_out_kernel(const T* __restrict__ X0, const T* __restrict__ halo_in, T* __restrict__ halo_out,
+                                int B, int T_len, int d, int km1) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t per_b = (int64_t)km1 * d;
+  if (e >= (int64_t)B * per_b) return;
+  const int b = (int)(e / per_b);
+  const int j = (int)((e % per_b) / d);
+  const int c = (int)(e % d);
+  const int src = T_len - km1 + j;
+  T v = static_cast<T>(0.f);
+  if (src >= 0)
+    v = X0[((int64_t)b * T_len + src) * d + c];
+  else if (halo_in != nullptr)
+    v = halo_in[((int64_t)b * km1 + km1 + src) * d + c];
+  halo_out[e] = v;
 }
 
 // --------------------------------------------------------------------------- fp32 GEMM
@@ -204,12 +228,14 @@ __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmParams p) {
 // --------------------------------------------------------------------------- exclusive scan
 // In place over the stack: on entry W[b, i] holds Delta_i (already scaled by eta); on exit
 // W[b, i] = W0 + sum_{j<i} Delta_j and W_final[b] = W0 + sum_j Delta_j.
+// W_init (optional, [B, d, d_ff]): each sequence's own starting state instead of W0.
 __global__ void chunk_scan_f32_kernel(float* __restrict__ W, const float* __restrict__ W0,
-                                      float* __restrict__ W_final, int B, int n_chunks, int64_t df) {
+                                      float* __restrict__ W_final, int B, int n_chunks, int64_t df,
+                                      const float* __restrict__ W_init) {
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int b = blockIdx.y;
   if (e >= df) return;
-  float acc = W0[e];
+  float acc = W_init != nullptr ? W_init[(int64_t)b * df + e] : W0[e];
   float* w = W + (int64_t)b * n_chunks * df + e;
   for (int i = 0; i < n_chunks; ++i) {
     const float delta = w[(int64_t)i * df];
@@ -219,7 +245,8 @@ __global__ void chunk_scan_f32_kernel(float* __restrict__ W, const float* __rest
   W_final[(int64_t)b * df + e] = acc;
 }
 
-// W_final[b] = W0 (as fp32) for every sequence: the state of an empty sequence.
+// W_final[b] = W0 (as fp32) for every sequence: the state of an empty sequence.  (A resumed
+// empty call copies its fp32 state with cudaMemcpyAsync instead.)
 template <typename T>
 __global__ void broadcast_state_kernel(const T* __restrict__ W0, float* __restrict__ W_final, int64_t df) {
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

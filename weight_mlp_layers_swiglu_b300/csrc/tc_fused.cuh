@@ -10,7 +10,9 @@
 // Hand-off: after the TMA stores of a W_eff slice have completed, each epilogue warp makes
 // them visible (fence.proxy.async + a release add) on the slice's counter; an apply tile of
 // chunk i >= 1 waits (bounded) until all units of its sequence have published chunk i, then
-// fences (fence.proxy.async) before its TMA loads.  Chunk 0 is applied with W_down0 itself.
+// fences (fence.proxy.async) before its TMA loads.  Chunk 0 is applied with W_down0 itself,
+// or, when each sequence starts from its own state (a resumed call), with W_eff[b, 0], which
+// the state phase then writes and publishes like the other slices.
 // All CTAs are co-resident (cooperative launch, one CTA per SM), so these waits always end.
 #pragma once
 
@@ -34,8 +36,8 @@ constexpr int BAR_BYTES = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + BAR_BYTES;
 
 struct Params {
-  state::Params s;        // skip_first = 1: W_eff[b, 0] is never written
-  gemm::Params a;         // Apply tiling, first_from_w0 = 1
+  state::Params s;        // skip_first = 1 (W_eff[b, 0] not written) unless s.W_init is given
+  gemm::Params a;         // Apply tiling; first_from_w0 = s.skip_first
   uint32_t* ready;        // [B * n_chunks]: published (unit, epilogue warp) snapshots of each slice
   uint32_t* next_tile;    // apply-tile queue head
   uint32_t ready_target;  // m_units * n_units * 4
@@ -198,7 +200,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       gemm::decode_tile(A, tile, prob, mt, nt);
       const int b = prob / A.n_chunks;
       const int i = prob - b * A.n_chunks;
-      if (i > 0) {
+      const bool from_w0 = i == 0 && A.first_from_w0;
+      if (!from_w0) {
         if (!wait_counter(&p.ready[prob], p.ready_target, A.st, abort_flag, 0x403)) break;
         fence_proxy_async_global();
       }
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive_expect_tx(&full[p_stage], STAGE_BYTES);
         const int k0 = kb * gemm::BK;
         tma_load_3d(sa, &map_za, &full[p_stage], k0, i * A.C + mt * gemm::BM, b);
-        if (i == 0)
+        if (from_w0)
           tma_load_2d(sb, &map_w0, &full[p_stage], k0, nt * gemm::BN);
         else
           tma_load_3d(sb, &map_weff_ld, &full[p_stage], k0, nt * gemm::BN, prob);
@@ -330,29 +333,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int b, mb, nb;
         state::decode_unit(S, u, b, mb, nb);
         const int row = mb * state::BMD + r_in_tile;
-        const bool row_ok = row < S.d;
         const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * state::BNF);
-        const __nv_bfloat16* src = S.W0 + (int64_t)row * S.f;
 #pragma unroll 1
         for (int c = 0; c < state::BNF / 32; ++c) {
-          const int col = nb * state::BNF + c * 32;
           uint32_t r[32];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_ok && col + g * 8 < S.f) w = *reinterpret_cast<const uint4*>(src + col + g * 8);
-            r[g * 8 + 0] = __float_as_uint(bf16_lo(w.x));
-            r[g * 8 + 1] = __float_as_uint(bf16_hi(w.x));
-            r[g * 8 + 2] = __float_as_uint(bf16_lo(w.y));
-            r[g * 8 + 3] = __float_as_uint(bf16_hi(w.y));
-            r[g * 8 + 4] = __float_as_uint(bf16_lo(w.z));
-            r[g * 8 + 5] = __float_as_uint(bf16_hi(w.z));
-            r[g * 8 + 6] = __float_as_uint(bf16_lo(w.w));
-            r[g * 8 + 7] = __float_as_uint(bf16_hi(w.w));
-          }
+          state::load_init32(S, b, row, nb * state::BNF + c * 32, r);
           tmem_st32(t_row + c * 32, r);
         }
         tmem_st_wait();
+        if (!S.skip_first) {  // per-sequence starting state: W_eff[b, 0] is this state in bf16
+          const int slice = b * S.n_chunks;
+          state::snapshot_bf16(out, t_row, &map_weff_st, nb * state::BNF, mb * state::BMD + q * 32, slice);
+          if (lane == 0) bulk_wait_pending<4>();
+          if (pending >= 0) publish(pending);
+          pending = slice;
+        }
         tc_fence_before();
         mbar_arrive(&snap_done[slot]);
       }

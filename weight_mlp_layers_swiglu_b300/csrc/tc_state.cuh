@@ -42,8 +42,42 @@ struct Params {
   int m_units, n_units, units;  // units = B * n_units * m_units
   const __nv_bfloat16* W0;      // [d, f]; W_eff [B, n_chunks, d, f] and W_final [B, d, f] via tensor maps
   int skip_first;               // 1: W_eff[b, 0] (= W_down0) is not written (the apply reads W_down0)
+  const float* W_init;          // optional [B, d, f] fp32: each sequence's own starting state
   DevStatus st;
 };
+
+// The accumulator's starting value for state rows `row`, columns col .. col+31 of sequence b:
+// W_init[b] (fp32) when given, else W_down0 (bf16).
+__device__ __forceinline__ void load_init32(const Params& p, int b, int row, int col, uint32_t (&r)[32]) {
+  const bool row_ok = row < p.d;
+  if (p.W_init != nullptr) {
+    const float* src = p.W_init + ((int64_t)b * p.d + row) * p.f;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row_ok && col + g * 4 < p.f) v = *reinterpret_cast<const float4*>(src + col + g * 4);
+      r[g * 4 + 0] = __float_as_uint(v.x);
+      r[g * 4 + 1] = __float_as_uint(v.y);
+      r[g * 4 + 2] = __float_as_uint(v.z);
+      r[g * 4 + 3] = __float_as_uint(v.w);
+    }
+    return;
+  }
+  const __nv_bfloat16* src = p.W0 + (int64_t)row * p.f;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (row_ok && col + g * 8 < p.f) w = *reinterpret_cast<const uint4*>(src + col + g * 8);
+    r[g * 8 + 0] = __float_as_uint(bf16_lo(w.x));
+    r[g * 8 + 1] = __float_as_uint(bf16_hi(w.x));
+    r[g * 8 + 2] = __float_as_uint(bf16_lo(w.y));
+    r[g * 8 + 3] = __float_as_uint(bf16_hi(w.y));
+    r[g * 8 + 4] = __float_as_uint(bf16_lo(w.z));
+    r[g * 8 + 5] = __float_as_uint(bf16_hi(w.z));
+    r[g * 8 + 6] = __float_as_uint(bf16_lo(w.w));
+    r[g * 8 + 7] = __float_as_uint(bf16_hi(w.w));
+  }
+}
 
 // Reads the 256 accumulator columns of this thread's TMEM lane and stores them as bf16
 // W_eff rows (4 boxes of 64 columns) for state rows y.. y+31 of slice z.
@@ -232,26 +266,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int b, mb, nb;
         decode_unit(p, u, b, mb, nb);
         const int row = mb * BMD + r_in_tile;
-        const bool row_ok = row < p.d;
         const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BNF);
-        const __nv_bfloat16* src = p.W0 + (int64_t)row * p.f;
 #pragma unroll 1
         for (int c = 0; c < BNF / 32; ++c) {
-          const int col = nb * BNF + c * 32;
           uint32_t r[32];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_ok && col + g * 8 < p.f) w = *reinterpret_cast<const uint4*>(src + col + g * 8);
-            r[g * 8 + 0] = __float_as_uint(bf16_lo(w.x));
-            r[g * 8 + 1] = __float_as_uint(bf16_hi(w.x));
-            r[g * 8 + 2] = __float_as_uint(bf16_lo(w.y));
-            r[g * 8 + 3] = __float_as_uint(bf16_hi(w.y));
-            r[g * 8 + 4] = __float_as_uint(bf16_lo(w.z));
-            r[g * 8 + 5] = __float_as_uint(bf16_hi(w.z));
-            r[g * 8 + 6] = __float_as_uint(bf16_lo(w.w));
-            r[g * 8 + 7] = __float_as_uint(bf16_hi(w.w));
-          }
+          load_init32(p, b, row, nb * BNF + c * 32, r);
           tmem_st32(t_row + c * 32, r);
         }
         tmem_st_wait();

@@ -40,6 +40,9 @@ _SIGNATURES = {
                                   [c_i64] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "ipttt_layer_forward": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                                                      c_vp, c_vp, c_vp, ctypes.c_size_t]),
+    "ipttt_layer_forward_resume": (ctypes.c_int, [c_vp] * 9 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float,
+                                                                            ctypes.c_int, c_vp, c_vp, c_vp, c_vp,
+                                                                            ctypes.c_size_t]),
     "ipttt_layer_forward_host": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float,
                                                                           ctypes.c_int, c_vp, c_vp, c_vp,
                                                                           ctypes.c_size_t]),
@@ -211,6 +214,40 @@ class Context:
         self._check(st, "layer_forward")
         return O, W_final
 
+    def layer_resume(self, H, X0, W_gate, W_up, W_target, conv_w, W_state, X0_halo, C: int, eta: float,
+                     O=None, W_state_out=None, X0_halo_out=None, workspace=None):
+        """Continue B sequences from their fp32 state and X0 halo (None = a new sequence's zeros).
+
+        Returns O [B,T,d], the new state [B,d,d_ff] (fp32) and the new halo [B,k-1,d]."""
+        B, T, d = H.shape
+        f = W_gate.shape[0]
+        k = conv_w.shape[1]
+        dt, dev = H.dtype, self.device
+        for t, n, s in ((H, "H", (B, T, d)), (X0, "X0", (B, T, d)), (W_gate, "W_gate", (f, d)),
+                        (W_up, "W_up", (f, d)), (W_target, "W_target", (d, d)), (conv_w, "conv_w", (d, k))):
+            _need(t, n, s, dt, dev)
+        _need(W_state, "W_state", (B, d, f), torch.float32, dev)
+        if X0_halo is not None:
+            _need(X0_halo, "X0_halo", (B, k - 1, d), dt, dev)
+        if O is None:
+            O = torch.empty((B, T, d), dtype=dt, device=dev)
+        if W_state_out is None:
+            W_state_out = torch.empty((B, d, f), dtype=torch.float32, device=dev)
+        if X0_halo_out is None:
+            X0_halo_out = torch.empty((B, k - 1, d), dtype=dt, device=dev)
+        _need(O, "O", (B, T, d), dt, dev)
+        _need(W_state_out, "W_state_out", (B, d, f), torch.float32, dev)
+        _need(X0_halo_out, "X0_halo_out", (B, k - 1, d), dt, dev)
+        code = dtype_code(dt)
+        ws = workspace if workspace is not None else self.workspace(B, T, d, f, C, k, code)
+        st = self.lib.ipttt_layer_forward_resume(
+            self.h, _ptr(H), _ptr(X0), _ptr(W_gate), _ptr(W_up), _ptr(W_target), _ptr(conv_w), _ptr(W_state),
+            _ptr(X0_halo) if X0_halo is not None else c_vp(0), B, T, d, f, C, k, float(eta), code, _ptr(O),
+            _ptr(W_state_out), _ptr(X0_halo_out) if X0_halo_out.numel() else c_vp(0), _ptr(ws),
+            ws.numel() * ws.element_size())
+        self._check(st, "layer_resume")
+        return O, W_state_out, X0_halo_out
+
     def layer_forward_host(self, H_host, X0_host, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float,
                            O_host, W_final_host, workspace=None):
         """The layer with H, X0, O, W_final in (pinned) host memory; asynchronous until sync()."""
@@ -308,3 +345,28 @@ class Context:
 
     def selftest_wait_timeout(self):
         self._check(self.lib.ipttt_selftest_wait_timeout(self.h), "selftest_wait_timeout")
+
+
+class StreamingLayer:
+    """Keeps the per-sequence fast-weight state and conv halo of B sequences across calls.
+
+    Each call to step() runs the layer on the next tokens of every sequence, continuing from the
+    state the previous call left; cutting a sequence at multiples of C gives exactly the results
+    of one call over the whole sequence.  Buffers only: all compute runs in the library.
+    """
+
+    def __init__(self, ctx: Context, W_gate, W_up, W_down0, W_target, conv_w, B: int, C: int, eta: float):
+        self.ctx, self.C, self.eta = ctx, C, eta
+        self.W_gate, self.W_up, self.W_target, self.conv_w = W_gate, W_up, W_target, conv_w
+        d, f = W_down0.shape
+        k = conv_w.shape[1]
+        self.state = W_down0.float().unsqueeze(0).expand(B, d, f).contiguous()
+        self.halo = torch.zeros((B, k - 1, d), dtype=W_down0.dtype, device=W_down0.device)
+        self._halo_next = torch.empty_like(self.halo)
+
+    def step(self, H, X0, O=None):
+        O, self.state, self._halo_next = self.ctx.layer_resume(
+            H, X0, self.W_gate, self.W_up, self.W_target, self.conv_w, self.state, self.halo, self.C, self.eta,
+            O=O, W_state_out=self.state, X0_halo_out=self._halo_next)
+        self.halo, self._halo_next = self._halo_next, self.halo
+        return O
