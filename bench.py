@@ -478,6 +478,9 @@ def main(argv=None):
                     help="tokens per call of the streaming leg (0 = skip it)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (a shorter case of the same shapes, e.g. for profiler captures)")
+    ap.add_argument("--sweep", choices=["chunk", "state"], default=None,
+                    help="one line per chunk size C in {256, 512, 1024, 2048} (eta = 1/C) or per state size "
+                         "d_ff in {0.5, 1, 4} x the workload's (the axes of the pages' ablations)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -488,6 +491,15 @@ def main(argv=None):
         w = w.with_(name=f"{w.name}_T{args.tokens}", T=args.tokens)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.sweep:
+        args.no_e2e, args.no_cpu_baseline, args.stream_tokens = True, True, 0
+        if args.sweep == "chunk":
+            points = [w.with_(name=f"{w.name}_C{c}", C=c, eta=1.0 / c) for c in (256, 512, 1024, 2048)]
+        else:
+            points = [w.with_(name=f"{w.name}_dff{int(m * w.d_ff)}", d_ff=int(m * w.d_ff)) for m in (0.5, 1.0, 4.0)]
+        for pw in points:
+            run_ours(args, pw)
+        return 0
     return run_ours(args, w)
 
 

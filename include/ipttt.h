@@ -94,6 +94,14 @@ ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* cuda_stream);
  * cooperative launch always use two. */
 ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable);
 
+/* Ablation variant of the target (zhichai.net page §6, conv/proj ablation; its Theorem 1 uses
+ * the next token's embedding as target): shift = 1 moves the conv window one token later, so
+ * that the target of token t ends at X0[t+1] (the token after a call's last one reads as
+ * zero, so split calls no longer match one call); shift = 0 (default) is the causal window.
+ * The other ablations need no switch: W_target = NULL is "w/o Proj" (identity projection;
+ * the projection GEMM is skipped), k = 1 with conv_w = 1 is "w/o Conv". */
+ipttt_status ipttt_set_target_shift(ipttt_ctx* ctx, int shift);
+
 /* Limit, in nanoseconds, on every device-side wait of later launches (default 2e9). */
 ipttt_status ipttt_set_wait_limit_ns(ipttt_ctx* ctx, uint64_t ns);
 
@@ -120,7 +128,7 @@ ipttt_status ipttt_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff,
  *   W_gate    [d_ff, d]        dtype, device      frozen, shared by all sequences
  *   W_up      [d_ff, d]        dtype, device      frozen
  *   W_down0   [d, d_ff]        dtype, device      initial fast weight
- *   W_target  [d, d]           dtype, device      [d_in, d_out], V = Y W_target
+ *   W_target  [d, d]           dtype, device      [d_in, d_out], V = Y W_target; NULL = identity
  *   conv_w    [d, k]           dtype, device      depthwise causal taps
  *   O         [B, T, d]        dtype, device      output
  *   W_final   [B, d, d_ff]     fp32,  device      state after the last chunk's update
@@ -182,7 +190,8 @@ ipttt_status ipttt_swiglu(ipttt_ctx* ctx, const void* H, const void* W_gate, con
                           int64_t rows, int64_t d, int64_t d_ff, ipttt_dtype dtype, void* Z);
 
 /* Step (2), §3.3: Y = CausalConv1D(X0) (per sequence), V = scale * (Y W_target).
- * X0 [B,T,d], conv_w [d,k], W_target [d,d], Y (scratch, written) [B,T,d], V [B,T,d]. */
+ * X0 [B,T,d], conv_w [d,k], W_target [d,d], Y (scratch, written) [B,T,d], V [B,T,d].
+ * W_target = NULL: V = scale * Y written directly (Y may then be NULL). */
 ipttt_status ipttt_target(ipttt_ctx* ctx, const void* X0, const void* conv_w, const void* W_target,
                           int64_t B, int64_t T, int64_t d, int k, float scale, ipttt_dtype dtype,
                           void* Y, void* V);

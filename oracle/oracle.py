@@ -72,27 +72,33 @@ def swiglu(H, W_gate, W_up) -> np.ndarray:
     return silu(H @ W_gate.T) * (H @ W_up.T)
 
 
-def causal_conv(X0, conv_w, halo=None) -> np.ndarray:
+def causal_conv(X0, conv_w, halo=None, shift: int = 0) -> np.ndarray:
     """Y = causal depthwise Conv1D(X0)  ([zhichai] §3.3, target equation, "causal padding").
 
-    X0: [T, d]; conv_w: [d, k].  Y[t, c] = sum_s conv_w[c, s] * X0[t - (k-1) + s, c].
+    X0: [T, d]; conv_w: [d, k].  Y[t, c] = sum_s conv_w[c, s] * X0[t + shift - (k-1) + s, c].
     Token indices before 0 read `halo` ([k-1, d], the k-1 tokens that precede X0 when a
     sequence is processed in several calls) or are zero (left padding of k-1) without one.
+    shift = 1 is the ablation variant whose window ends at the next token t+1 (the page
+    describes the kernel size as setting how far ahead the target looks, and its Theorem 1
+    uses the next token's embedding); the token after the last one reads as zero.
     """
     X0, conv_w = _f64(X0), _f64(conv_w)
     T, d = X0.shape
     k = conv_w.shape[1]
     pad = np.zeros((k - 1, d)) if halo is None else _f64(halo).reshape(k - 1, d)
-    Xp = np.concatenate([pad, X0])  # Xp[t + k - 1] = X0[t]
+    Xp = np.concatenate([pad, X0, np.zeros((shift, d))])  # Xp[t + k - 1] = X0[t]
     Y = np.zeros((T, d))
     for s in range(k):
-        Y += conv_w[:, s] * Xp[s: s + T]
+        Y += conv_w[:, s] * Xp[s + shift: s + shift + T]
     return Y
 
 
-def target(X0, conv_w, W_target, halo=None) -> np.ndarray:
-    """V = Conv1D(X0) W_target  ([zhichai] §3.3, LM-aligned target).  Returns [T, d]."""
-    return causal_conv(X0, conv_w, halo) @ _f64(W_target)
+def target(X0, conv_w, W_target, halo=None, shift: int = 0) -> np.ndarray:
+    """V = Conv1D(X0) W_target  ([zhichai] §3.3, LM-aligned target).  Returns [T, d].
+
+    W_target None is the "w/o Proj" ablation (identity projection, [zhichai] §6 table)."""
+    Y = causal_conv(X0, conv_w, halo, shift)
+    return Y if W_target is None else Y @ _f64(W_target)
 
 
 def chunk_delta(V, Z) -> np.ndarray:
@@ -109,7 +115,8 @@ def chunk_rows(T: int, C: int):
     return [(s, min(s + C, T)) for s in range(0, T, C)]
 
 
-def sequence_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, halo=None):
+def sequence_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, halo=None,
+                     shift: int = 0):
     """One sequence, the literal sequential chunk loop.
 
     For each chunk in order: the chunk's output is computed with the current
@@ -120,7 +127,7 @@ def sequence_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta
     before it (see causal_conv).  Returns O [T, d] and the final W_down [d, d_ff].
     """
     Z = swiglu(H, W_gate, W_up)
-    V = target(X0, conv_w, W_target, halo)
+    V = target(X0, conv_w, W_target, halo, shift)
     W = _f64(W_down0).copy()
     T = Z.shape[0]
     O = np.zeros((T, W.shape[0]))
@@ -130,7 +137,7 @@ def sequence_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta
     return O, W
 
 
-def layer_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float):
+def layer_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, shift: int = 0):
     """Batched layer: H, X0 [B, T, d] -> O [B, T, d], final W_down [B, d, d_ff].
 
     The sequences of a batch are independent; each carries its own fast-weight
@@ -144,7 +151,8 @@ def layer_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: f
     O = np.zeros((B, T, d))
     Wf = np.zeros((B, d, f))
     for b in range(B):
-        O[b], Wf[b] = sequence_forward(H[b], X0[b], W_gate, W_up, W_down0, W_target, conv_w, C, eta)
+        O[b], Wf[b] = sequence_forward(H[b], X0[b], W_gate, W_up, W_down0, W_target, conv_w, C, eta,
+                                       shift=shift)
     return O, Wf
 
 

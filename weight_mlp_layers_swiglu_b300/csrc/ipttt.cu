@@ -54,6 +54,7 @@ struct ipttt_ctx {
   bool attrs_set = false;
   bool coop = false;       // device supports cooperative launches
   bool fused_tail = true;  // run steps (3)-(5) as one cooperative kernel when possible
+  int target_shift = 0;    // 1: the conv window of the target ends at the next token
   // The causal conv runs on an internal side stream, forked from and joined back into
   // `stream` with these events, so that it overlaps the SwiGLU GEMM.
   cudaStream_t side = nullptr;
@@ -306,14 +307,14 @@ ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const voi
 
 template <typename E>
 void launch_conv(ipttt_ctx* ctx, dim3 grid, dim3 block, const void* X0, const void* cw, void* Y, int T_len, int d,
-                 int k, const void* halo) {
+                 int k, const void* halo, int shift, float scale) {
   const E* x = static_cast<const E*>(X0);
   const E* w = static_cast<const E*>(cw);
   E* y = static_cast<E*>(Y);
   const E* h = static_cast<const E*>(halo);
   switch (k) {
 #define IPTTT_CONV_CASE(KK) \
-  case KK: simt::causal_conv_kernel<E, KK><<<grid, block, 0, ctx->stream>>>(x, w, y, T_len, d, h); break;
+  case KK: simt::causal_conv_kernel<E, KK><<<grid, block, 0, ctx->stream>>>(x, w, y, T_len, d, h, shift, scale); break;
     IPTTT_CONV_CASE(1) IPTTT_CONV_CASE(2) IPTTT_CONV_CASE(3) IPTTT_CONV_CASE(4)
     IPTTT_CONV_CASE(5) IPTTT_CONV_CASE(6) IPTTT_CONV_CASE(7) IPTTT_CONV_CASE(8)
 #undef IPTTT_CONV_CASE
@@ -321,15 +322,16 @@ void launch_conv(ipttt_ctx* ctx, dim3 grid, dim3 block, const void* X0, const vo
   }
 }
 
+// Y = scale * CausalConv1D(X0), window shifted by ctx->target_shift (0 or 1).
 ipttt_status run_conv(ipttt_ctx* ctx, const void* X0, const void* cw, int64_t B, int64_t T, int64_t d, int k,
-                      ipttt_dtype dt, void* Y, const void* halo = nullptr) {
+                      ipttt_dtype dt, void* Y, const void* halo = nullptr, float scale = 1.f) {
   if (B == 0 || T == 0) return IPTTT_OK;
   dim3 block(32, 4);
   dim3 grid(ceil_div(d / 8, 32), ceil_div(T, (int64_t)simt::CONV_TS * 4), (unsigned)B);
   if (dt == IPTTT_BF16)
-    launch_conv<__nv_bfloat16>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k, halo);
+    launch_conv<__nv_bfloat16>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k, halo, ctx->target_shift, scale);
   else
-    launch_conv<float>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k, halo);
+    launch_conv<float>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k, halo, ctx->target_shift, scale);
   return check_launch(ctx, "conv launch");
 }
 
@@ -601,7 +603,9 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
     cudaStream_t main_stream = ctx->stream;
     ctx->stream = ctx->side;
     mark(ctx, call, kEvConvStart, ctx->side);
-    s = run_conv(ctx, X0, cw, B, T, d, k, dt, Y, halo_in);
+    // without W_target (the "w/o Proj" ablation) the conv writes V = eta * conv(X0) directly
+    s = Wt != nullptr ? run_conv(ctx, X0, cw, B, T, d, k, dt, Y, halo_in)
+                      : run_conv(ctx, X0, cw, B, T, d, k, dt, V, halo_in, eta);
     mark(ctx, call, kEvConvEnd, ctx->side);
     ctx->stream = main_stream;
     if (s != IPTTT_OK) return s;
@@ -615,8 +619,13 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   const bool fuse = bf16 && ctx->fused_tail && ctx->coop;
   uint32_t* ctr = reinterpret_cast<uint32_t*>(base + L.ctr);
   const int n_ctr = (int)(B * n_chunks_of(T, C) + 1);
-  if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V, fuse ? ctr : nullptr, fuse ? n_ctr : 0)) != IPTTT_OK)
-    return s;
+  if (Wt != nullptr) {
+    if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V, fuse ? ctr : nullptr, fuse ? n_ctr : 0)) != IPTTT_OK)
+      return s;
+  } else if (fuse) {
+    const cudaError_t ez = cudaMemsetAsync(ctr, 0, (size_t)n_ctr * sizeof(uint32_t), ctx->stream);
+    if (ez != cudaSuccess) return cuda_fail(ctx, ez, "counter reset");
+  }
   mark(ctx, call, kEvTargetEnd, ctx->stream);
   if (fuse) {
     if ((s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr, W_init)) != IPTTT_OK)
@@ -631,7 +640,8 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
     if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, w0_first)) != IPTTT_OK) return s;
     mark(ctx, call, kEvApplyEnd, ctx->stream);
   }
-  if (call >= 0) ctx->timed_launches += (bf16 ? (fuse ? 4 : 5) : 6) + ((halo_out != nullptr && k > 1) ? 1 : 0);
+  if (call >= 0)
+    ctx->timed_launches += (bf16 ? (fuse ? 4 : 5) : 6) + ((halo_out != nullptr && k > 1) ? 1 : 0) - (Wt ? 0 : 1);
   return IPTTT_OK;
 }
 
@@ -654,7 +664,7 @@ ipttt_status validate_layer(ipttt_ctx* ctx, const void* H, const void* X0, const
     const char* n;
     bool needed;
   } ptrs[] = {{H, "H", T > 0},        {X0, "X0", T > 0},  {Wg, "W_gate", T > 0}, {Wu, "W_up", T > 0},
-              {W0, "W_down0", true},  {Wt, "W_target", T > 0}, {cw, "conv_w", T > 0}, {O, "O", T > 0},
+              {W0, "W_down0", true},  {Wt, "W_target", false}, {cw, "conv_w", T > 0}, {O, "O", T > 0},
               {W_final, "W_final", true}, {ws, "workspace", T > 0}};
   for (const P& q : ptrs) {
     if (!q.needed) continue;
@@ -666,6 +676,10 @@ ipttt_status validate_layer(ipttt_ctx* ctx, const void* H, const void* X0, const
       set_err(ctx, "%s is not 16-byte aligned", q.n);
       return IPTTT_ERR_INVALID_ARG;
     }
+  }
+  if (Wt != nullptr && !aligned16(Wt)) {
+    set_err(ctx, "W_target is not 16-byte aligned");
+    return IPTTT_ERR_INVALID_ARG;
   }
   const WsLayout L = ws_layout(B, T, d, f, C, dt);
   if (T > 0 && ws_bytes < L.total) {
@@ -771,6 +785,16 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
 ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* stream) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
   ctx->stream = static_cast<cudaStream_t>(stream);
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_set_target_shift(ipttt_ctx* ctx, int shift) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  if (shift != 0 && shift != 1) {
+    set_err(ctx, "target shift must be 0 or 1 (got %d)", shift);
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  ctx->target_shift = shift;
   return IPTTT_OK;
 }
 
@@ -981,7 +1005,7 @@ ipttt_status ipttt_target(ipttt_ctx* ctx, const void* X0, const void* conv_w, co
   ipttt_status s = check_shape(ctx, B, T, d, 8, 1, k, dt, false);
   if (s != IPTTT_OK) return s;
   if (B == 0 || T == 0) return IPTTT_OK;
-  if (!X0 || !conv_w || !W_target || !Y || !V || !aligned16(X0) || !aligned16(W_target) || !aligned16(Y) ||
+  if (!X0 || !conv_w || !V || !aligned16(X0) || (W_target && (!aligned16(W_target) || !Y || !aligned16(Y))) ||
       !aligned16(V)) {
     set_err(ctx, "target: NULL or misaligned pointer");
     return IPTTT_ERR_INVALID_ARG;
@@ -992,6 +1016,7 @@ ipttt_status ipttt_target(ipttt_ctx* ctx, const void* X0, const void* conv_w, co
   }
   DeviceGuard g(ctx->device);
   if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  if (W_target == nullptr) return run_conv(ctx, X0, conv_w, B, T, d, k, dt, V, nullptr, scale);
   if ((s = run_conv(ctx, X0, conv_w, B, T, d, k, dt, Y)) != IPTTT_OK) return s;
   return run_target_gemm(ctx, Y, W_target, B * T, d, scale, dt, V);
 }

@@ -53,10 +53,12 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const fl
 }
 
 // halo (optional, [B, K-1, d]): the K-1 rows that precede X0's first token of each sequence
-// (rows of an earlier call); without it those rows are zero.
+// (rows of an earlier call); without it those rows are zero.  shift = 1 moves the window one
+// token later (it ends at t+1; the token after the last one reads as zero).  The output is
+// multiplied by `scale`.
 template <typename T, int K>
 __global__ void causal_conv_kernel(const T* __restrict__ X0, const T* __restrict__ conv_w, T* __restrict__ Y,
-                                   int T_len, int d, const T* __restrict__ halo) {
+                                   int T_len, int d, const T* __restrict__ halo, int shift, float scale) {
   const int cg = blockIdx.x * blockDim.x + threadIdx.x;  // channel group of 8
   const int c0 = cg * 8;
   const int t0 = (blockIdx.y * blockDim.y + threadIdx.y) * CONV_TS;
@@ -69,14 +71,14 @@ __global__ void causal_conv_kernel(const T* __restrict__ X0, const T* __restrict
     for (int s = 0; s < K; ++s) w[e][s] = static_cast<float>(conv_w[(int64_t)(c0 + e) * K + s]);
   const T* xb = X0 + (int64_t)b * T_len * d + c0;
   T* yb = Y + (int64_t)b * T_len * d + c0;
-  // win[s] holds X0[t-(K-1)+s], s < K-1, while output t is formed; win[K-1] is the current token
+  // win[s] holds X0[t+shift-(K-1)+s], s < K-1, while output t is formed; win[K-1] is X0[t+shift]
   float win[K][8];
 #pragma unroll
   for (int s = 0; s < K - 1; ++s) {
-    const int src = t0 - (K - 1) + s;
-    if (src >= 0) {
+    const int src = t0 + shift - (K - 1) + s;
+    if (src >= 0 && src < T_len) {
       load8<T>(xb + (int64_t)src * d, win[s]);
-    } else if (halo != nullptr) {
+    } else if (src < 0 && halo != nullptr) {
       load8<T>(halo + ((int64_t)b * (K - 1) + (K - 1) + src) * d + c0, win[s]);
     } else {
 #pragma unroll
@@ -85,14 +87,19 @@ __global__ void causal_conv_kernel(const T* __restrict__ X0, const T* __restrict
   }
   const int t_end = min(t0 + CONV_TS, T_len);
   for (int t = t0; t < t_end; ++t) {
-    load8<T>(xb + (int64_t)t * d, win[K - 1]);
+    if (t + shift < T_len) {
+      load8<T>(xb + (int64_t)(t + shift) * d, win[K - 1]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) win[K - 1][e] = 0.f;
+    }
     float out[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       float acc = 0.f;
 #pragma unroll
       for (int s = 0; s < K; ++s) acc = fmaf(w[e][s], win[s][e], acc);
-      out[e] = acc;
+      out[e] = acc * scale;
     }
     store8<T>(yb + (int64_t)t * d, out);
 #pragma unroll

@@ -32,6 +32,7 @@ _SIGNATURES = {
     "ipttt_set_stream": (ctypes.c_int, [c_vp, c_vp]),
     "ipttt_set_wait_limit_ns": (ctypes.c_int, [c_vp, ctypes.c_uint64]),
     "ipttt_set_fused_tail": (ctypes.c_int, [c_vp, ctypes.c_int]),
+    "ipttt_set_target_shift": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_sync": (ctypes.c_int, [c_vp]),
     "ipttt_last_error": (ctypes.c_char_p, [c_vp]),
     "ipttt_destroy": (None, [c_vp]),
@@ -162,6 +163,9 @@ class Context:
         self.stream = stream
         self._check(self.lib.ipttt_set_stream(self.h, c_vp(stream.cuda_stream)), "set_stream")
 
+    def set_target_shift(self, shift: int):
+        self._check(self.lib.ipttt_set_target_shift(self.h, int(shift)), "set_target_shift")
+
     def set_fused_tail(self, enable: bool):
         self._check(self.lib.ipttt_set_fused_tail(self.h, 1 if enable else 0), "set_fused_tail")
 
@@ -197,9 +201,10 @@ class Context:
         k = conv_w.shape[1]
         dt, dev = H.dtype, self.device
         for t, n, s in ((H, "H", (B, T, d)), (X0, "X0", (B, T, d)), (W_gate, "W_gate", (f, d)),
-                        (W_up, "W_up", (f, d)), (W_down0, "W_down0", (d, f)), (W_target, "W_target", (d, d)),
-                        (conv_w, "conv_w", (d, k))):
+                        (W_up, "W_up", (f, d)), (W_down0, "W_down0", (d, f)), (conv_w, "conv_w", (d, k))):
             _need(t, n, s, dt, dev)
+        if W_target is not None:
+            _need(W_target, "W_target", (d, d), dt, dev)
         code = dtype_code(dt)
         if O is None:
             O = torch.empty((B, T, d), dtype=dt, device=dev)
@@ -209,7 +214,7 @@ class Context:
         _need(W_final, "W_final", (B, d, f), torch.float32, dev)
         ws = workspace if workspace is not None else self.workspace(B, T, d, f, C, k, code)
         st = self.lib.ipttt_layer_forward(self.h, _ptr(H), _ptr(X0), _ptr(W_gate), _ptr(W_up), _ptr(W_down0),
-                                          _ptr(W_target), _ptr(conv_w), B, T, d, f, C, k, float(eta), code,
+                                          _ptr(W_target) if W_target is not None else c_vp(0), _ptr(conv_w), B, T, d, f, C, k, float(eta), code,
                                           _ptr(O), _ptr(W_final), _ptr(ws), ws.numel() * ws.element_size())
         self._check(st, "layer_forward")
         return O, W_final
