@@ -344,6 +344,60 @@ def stream_leg(args, w, ctx, weights, H, X0, dev, world):
             "unit": UNIT, "ms_per_sequence": ms}
 
 
+def run_cp(args, w):
+    """Context parallelism: rank r runs tokens [r*T_r, (r+1)*T_r) of every sequence; one step is
+    the three-step scheme over all ranks (strong scaling: the job processes B*T tokens per step)."""
+    import torch
+    import torch.distributed as dist
+
+    import weight_mlp_layers_swiglu_b300 as pkg
+    from weight_mlp_layers_swiglu_b300 import context_parallel as cp
+    from weight_mlp_layers_swiglu_b300.inputs import make_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist.init_process_group("nccl" if world > 1 else "gloo", device_id=dev if world > 1 else None,
+                            rank=rank, world_size=world,
+                            init_method=None if world > 1 else "tcp://127.0.0.1:29517")
+    T_r = -(-w.T // world // w.C) * w.C
+    lo, hi = rank * T_r, min((rank + 1) * T_r, w.T)
+    x = make_inputs(w)
+    H = x["H"][:, lo:hi].contiguous().to(dev)
+    X0 = x["X0"][:, lo:hi].contiguous().to(dev)
+    wd = {k: v.to(dev) for k, v in x.items() if k not in ("H", "X0")}
+    ctx = pkg.Context(local)
+    lt, lr = cp.library_locals(ctx, wd["W_gate"], wd["W_up"], wd["W_target"], wd["conv_w"], w.C, w.eta)
+
+    def step():
+        return cp.cp_forward(H, X0, wd["W_down0"], w.k, lt, lr)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    if ctx.sync() != 0:
+        raise RuntimeError(ctx.last_error())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev if world > 1 else None)
+    if rank == 0:
+        print(json.dumps({"metric": METRIC, "value": w.B * w.T * args.steps / (ms * 1e-3), "unit": UNIT,
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "strong",
+                          "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+                          "config": workload_config(w) | {"parallelism": f"context parallel x{world}",
+                                                          "tokens_per_rank": T_r}}), flush=True)
+    ctx.close()
+    dist.destroy_process_group()
+    return 0
+
+
 def e2e_leg(args, w, ctx, weights, H_host, X_host, dev, world):
     """The same metric end to end through the C ABI with host buffers: every step uploads H and
     X0 from pinned memory, runs the layer and downloads O and W_final."""
@@ -478,6 +532,9 @@ def main(argv=None):
                     help="tokens per call of the streaming leg (0 = skip it)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (a shorter case of the same shapes, e.g. for profiler captures)")
+    ap.add_argument("--cp", action="store_true",
+                    help="context parallelism under torchrun: each rank holds a slice of every sequence "
+                         "(strong scaling; the exchange is one all_gather of the fp32 update totals)")
     ap.add_argument("--sweep", choices=["chunk", "state"], default=None,
                     help="one line per chunk size C in {256, 512, 1024, 2048} (eta = 1/C) or per state size "
                          "d_ff in {0.5, 1, 4} x the workload's (the axes of the pages' ablations)")
@@ -491,6 +548,8 @@ def main(argv=None):
         w = w.with_(name=f"{w.name}_T{args.tokens}", T=args.tokens)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.cp:
+        return run_cp(args, w)
     if args.sweep:
         args.no_e2e, args.no_cpu_baseline, args.stream_tokens = True, True, 0
         if args.sweep == "chunk":

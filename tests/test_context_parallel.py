@@ -1,0 +1,100 @@
+"""Context parallelism (the zhichai.net page's §3.2 three-step scheme) on CPU ranks.
+
+Each gloo rank holds a contiguous token range of every sequence and computes with the oracle;
+the exchange (one all_gather of the fp32 update totals, one of the k-1 halo rows) runs through
+weight_mlp_layers_swiglu_b300.context_parallel.  The concatenated outputs and the last rank's
+state must equal the oracle's single-process layer."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+from oracle import oracle
+from weight_mlp_layers_swiglu_b300 import context_parallel as cp
+from weight_mlp_layers_swiglu_b300.inputs import random_case
+
+CASE = dict(B=2, T=48, d=6, f=10, C=8, k=3, eta=0.3, dtype="f32", seed=17)
+
+
+def _oracle_locals(x, C, eta):
+    def local_total(H_r, X0_r, halo):
+        B, _, d = H_r.shape
+        zero = np.zeros((B, d, x["W_gate"].shape[0]))
+        _, S, _ = oracle.layer_resume(H_r, X0_r, x["W_gate"], x["W_up"], x["W_target"], x["conv_w"], zero, halo, C,
+                                      eta)
+        return torch.from_numpy(S)
+
+    def local_resume(H_r, X0_r, W_init, halo):
+        O, W, _ = oracle.layer_resume(H_r, X0_r, x["W_gate"], x["W_up"], x["W_target"], x["conv_w"], W_init, halo, C,
+                                      eta)
+        return torch.from_numpy(O), torch.from_numpy(W)
+
+    return local_total, local_resume
+
+
+def _inputs():
+    w, x = random_case(CASE["B"], CASE["T"], CASE["d"], CASE["f"], CASE["C"], CASE["k"], CASE["eta"], CASE["dtype"],
+                       CASE["seed"])
+    return w, {n: t.double() for n, t in x.items()}
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, T_r, q):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w, x = _inputs()
+    lo, hi = rank * T_r, min((rank + 1) * T_r, w.T)
+    lt, lr = _oracle_locals(x, w.C, w.eta)
+    O_r, W_r = cp.cp_forward(x["H"][:, lo:hi].contiguous(), x["X0"][:, lo:hi].contiguous(), x["W_down0"], w.k, lt, lr)
+    q.put((rank, O_r.numpy(), W_r.numpy()))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,T_r", [(2, 24), (3, 16), (3, 24)])
+def test_gloo_ranks_equal_the_single_process_layer(world, T_r):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, T_r, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = sorted([q.get(timeout=180) for _ in procs], key=lambda t: t[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    w, x = _inputs()
+    O_ref, W_ref = oracle.layer_forward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"],
+                                        x["conv_w"], w.C, w.eta)
+    O = np.concatenate([g[1] for g in got if g[1].shape[1] > 0], axis=1)
+    assert np.abs(O - O_ref).max() / np.abs(O_ref).max() < 1e-12
+    # the last rank that holds tokens carries the final state of the whole sequence
+    last = max(r for r in range(world) if r * T_r < w.T)
+    assert np.abs(got[last][2] - W_ref).max() / np.abs(W_ref).max() < 1e-12
+
+
+def test_emulated_ranks_and_the_prefix():
+    w, x = _inputs()
+    lt, lr = _oracle_locals(x, w.C, w.eta)
+    O, W = cp.cp_forward_emulated(x["H"], x["X0"], x["W_down0"], w.k, 3, 16, lt, lr)
+    O_ref, W_ref = oracle.layer_forward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"],
+                                        x["conv_w"], w.C, w.eta)
+    assert np.abs(O.numpy() - O_ref).max() / np.abs(O_ref).max() < 1e-12
+    assert np.abs(W.numpy() - W_ref).max() / np.abs(W_ref).max() < 1e-12
+    # the prefix of rank r sums exactly the totals of ranks < r
+    totals = [torch.full((2, 3, 4), float(q + 1)) for q in range(4)]
+    W0 = torch.zeros(3, 4)
+    assert torch.equal(cp.exclusive_prefix(W0, totals, 0), torch.zeros(2, 3, 4))
+    assert torch.equal(cp.exclusive_prefix(W0, totals, 3), torch.full((2, 3, 4), 6.0))
+    # the halo is the previous range's last k-1 rows
+    X = torch.arange(2 * 5 * 3, dtype=torch.float64).reshape(2, 5, 3)
+    assert torch.equal(cp.halo_rows(X, 3), X[:, 3:])

@@ -1,0 +1,35 @@
+"""Context parallelism on the GPU, ranks emulated one after another on one device (no kernel
+waits on another): the library computes each rank's total and its resumed range, the prefix
+and the halo are passed between them on the host side.  The result must meet the parity bar
+against the oracle, and stay close to one call of the layer (the per-rank totals sum the fp32
+state in a different order, so a few bf16 roundings may differ)."""
+import pytest
+import torch
+
+from tests.util import TOL, rel_err, to_dev
+from weight_mlp_layers_swiglu_b300.inputs import random_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dt,world,T_r", [("bf16", 2, 512), ("bf16", 4, 256), ("f32", 3, 192)])
+def test_emulated_ranks_match_one_call(dt, world, T_r):
+    import weight_mlp_layers_swiglu_b300 as pkg
+    from weight_mlp_layers_swiglu_b300 import context_parallel as cp
+
+    C = 128 if dt == "bf16" else 64
+    w, x = random_case(2, world * T_r - 40, 256, 512, C, 4, 4.0 / C, dt, 91)
+    xd = to_dev(x)
+    ctx = pkg.Context(0)
+    O_ref, W_ref = ctx.layer_forward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
+                                     xd["conv_w"], w.C, w.eta)
+    lt, lr = cp.library_locals(ctx, xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], w.C, w.eta)
+    O, W = cp.cp_forward_emulated(xd["H"], xd["X0"], xd["W_down0"], w.k, world, T_r, lt, lr)
+    assert ctx.sync() == 0, ctx.last_error()
+    ctx.close()
+    from oracle import oracle
+
+    O_or, W_or = oracle.layer_forward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"],
+                                      x["conv_w"], w.C, w.eta)
+    assert rel_err(O, O_or) <= TOL[dt] and rel_err(W, W_or) <= TOL[dt]
+    assert rel_err(O, O_ref) <= TOL[dt] and rel_err(W, W_ref) <= TOL[dt] / 20
