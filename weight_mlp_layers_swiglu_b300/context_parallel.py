@@ -60,6 +60,9 @@ def cp_forward(H_r, X0_r, W_down0, k: int, local_total: LocalTotal, local_resume
 
     world = dist.get_world_size(group)
     rank = dist.get_rank(group)
+    if world == 1:  # nothing to exchange
+        W_init = W_down0.float().unsqueeze(0).expand(H_r.shape[0], *W_down0.shape).contiguous()
+        return local_resume(H_r, X0_r, W_init, torch.zeros_like(halo_rows(X0_r, k)))
     my_halo = halo_rows(X0_r, k)
     halos = [torch.empty_like(my_halo) for _ in range(world)]
     dist.all_gather(halos, my_halo.contiguous(), group=group)
