@@ -182,6 +182,50 @@ ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const 
                                       ipttt_dtype dtype, void* O_host, float* W_final_host,
                                       void* workspace, size_t workspace_bytes);
 
+/* ---- backward pass ----
+ * The pages train the layer (§5 results: continued training of a 4B model, experiment 1, and
+ * pretraining from scratch, experiment 3) but print no gradient formulas; these are the exact
+ * derivatives of steps (1)-(5) by the chain rule, for a loss L(O, W_final).  With
+ * G_i = dO_i^T Z_i and R_i = dW_final + sum_{l>i} G_l (the gradient reaching the state after
+ * chunk i, an exclusive suffix sum: the forward's prefix scan run backwards):
+ *   dW_down0 = sum_b (dW_final[b] + sum_i G_i)
+ *   dZ_i     = dO_i W_i + eta V_i R_i              dV_i = eta Z_i R_i^T
+ *   dA, dU   = the SwiGLU adjoints of dZ            (A = H W_gate^T, U = H W_up^T)
+ *   dH = dA W_gate + dU W_up    dW_gate = dA^T H    dW_up = dU^T H
+ *   dY = dV W_target^T          dW_target = Y^T dV  (Y = CausalConv1D(X0))
+ *   dX0, dconv_w                the conv's adjoints (the window shift of
+ *                               ipttt_set_target_shift is honoured).
+ * The forward quantities (Z, A, U, Y, V and every W_i) are recomputed, not passed in. */
+
+/* Bytes of device workspace ipttt_layer_backward needs (host-only call).  Layout: Y, V [B,T,d],
+ * Z [B,T,d_ff], [A|U] [B,T,2*d_ff], dZ [B,T,d_ff], dV, dY [B,T,d], the W_i and R_i stacks
+ * [B,ceil(T/C),d,d_ff] (all dtype), per-sequence dW_down0 [B,d,d_ff] fp32 and the conv-tap
+ * partial sums [B*ceil(T/256),d,k] fp32; each region 256-byte aligned.  Errors as
+ * ipttt_workspace_size. */
+ipttt_status ipttt_backward_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
+                                           ipttt_dtype dtype, size_t* bytes);
+
+/* Gradients of the whole layer.  Inputs as ipttt_layer_forward, plus
+ *   dO        [B, T, d]        dtype, device      gradient of the loss w.r.t. O
+ *   dW_final  [B, d, d_ff]     fp32,  device      gradient w.r.t. W_final; NULL = zero
+ * Outputs (overwritten, never accumulated into):
+ *   dH, dX0   [B, T, d]        dtype, device
+ *   dW_gate, dW_up [d_ff, d]   fp32,  device      summed over the batch
+ *   dW_down0  [d, d_ff]        fp32,  device      summed over the batch
+ *   dW_target [d, d]           fp32,  device      NULL allowed (and ignored) iff W_target is NULL
+ *   dconv_w   [d, k]           fp32,  device
+ *   workspace                  device, >= ipttt_backward_workspace_size() bytes, overwritten
+ * bf16: every product on the tensor cores with fp32 accumulation; the intermediates (Z, V,
+ * W_i, R_i, dZ, dA, dU, dV, dY) are rounded to bf16 between steps.  B*T = 0 writes zeros
+ * (dW_down0 = sum_b dW_final[b]).  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                  const void* W_up, const void* W_down0, const void* W_target,
+                                  const void* conv_w, int64_t B, int64_t T, int64_t d, int64_t d_ff,
+                                  int64_t C, int k, float eta, ipttt_dtype dtype, const void* dO,
+                                  const float* dW_final, void* dH, void* dX0, float* dW_gate, float* dW_up,
+                                  float* dW_down0, float* dW_target, float* dconv_w, void* workspace,
+                                  size_t workspace_bytes);
+
 /* ---- the individual steps (the layer is exactly these calls in this order) ---- */
 
 /* Step (1), §3.1: Z[r] = SiLU(H[r] W_gate^T) * (H[r] W_up^T) for rows r < rows (rows = B*T).

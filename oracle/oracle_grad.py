@@ -22,15 +22,19 @@ def _t(x):
     return torch.as_tensor(x, dtype=torch.float64).clone()
 
 
-def forward_torch(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float):
-    """O [B, T, d] and final W_down [B, d, d_ff], torch float64, differentiable."""
+def forward_torch(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, shift: int = 0):
+    """O [B, T, d] and final W_down [B, d, d_ff], torch float64, differentiable.
+
+    W_target None is the identity projection and shift = 1 the conv window ending at the next
+    token (the ablation variants of the zhichai page's §6 table and its Theorem 1), as in
+    oracle.target."""
     B, T, d = H.shape
     k = conv_w.shape[1]
     A = H @ W_gate.T
     Z = A * torch.sigmoid(A) * (H @ W_up.T)
-    Xp = torch.cat([torch.zeros(B, k - 1, d, dtype=H.dtype), X0], dim=1)
-    Y = sum(conv_w[:, s] * Xp[:, s: s + T] for s in range(k))
-    V = Y @ W_target
+    Xp = torch.cat([torch.zeros(B, k - 1, d, dtype=H.dtype), X0, torch.zeros(B, shift, d, dtype=H.dtype)], dim=1)
+    Y = sum(conv_w[:, s] * Xp[:, s + shift: s + shift + T] for s in range(k))
+    V = Y if W_target is None else Y @ W_target
     outs, finals = [], []
     for b in range(B):
         W = W_down0
@@ -44,14 +48,17 @@ def forward_torch(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: f
     return torch.stack(outs), torch.stack(finals)
 
 
-def layer_backward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, dO, dW_final=None):
+def layer_backward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, dO, dW_final=None,
+                   shift: int = 0):
     """Gradients of <dO, O> + <dW_final, W_final> (dW_final None = 0) with respect to
-    H, X0, W_gate, W_up, W_down0, W_target, conv_w, as a dict of float64 tensors."""
+    H, X0, W_gate, W_up, W_down0, W_target, conv_w, as a dict of float64 tensors (W_target's
+    entry is None when W_target is None)."""
     names = ["H", "X0", "W_gate", "W_up", "W_down0", "W_target", "conv_w"]
-    leaves = {n: _t(v).requires_grad_(True) for n, v in zip(names, (H, X0, W_gate, W_up, W_down0, W_target, conv_w))}
-    O, Wf = forward_torch(*(leaves[n] for n in names), C, eta)
+    vals = (H, X0, W_gate, W_up, W_down0, W_target, conv_w)
+    leaves = {n: (None if v is None else _t(v).requires_grad_(True)) for n, v in zip(names, vals)}
+    O, Wf = forward_torch(*(leaves[n] for n in names), C, eta, shift)
     loss = (O * _t(dO)).sum()
     if dW_final is not None:
         loss = loss + (Wf * _t(dW_final)).sum()
     loss.backward()
-    return {n: leaves[n].grad.detach() for n in names}
+    return {n: (None if leaves[n] is None else leaves[n].grad.detach()) for n in names}

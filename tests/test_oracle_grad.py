@@ -85,3 +85,59 @@ def test_reverse_chunk_scan_reproduces_autograd():
         dH = dA @ x["W_gate"].numpy() + dU @ x["W_up"].numpy()
         assert np.abs(dH - grads["H"][b].numpy()).max() < 1e-10
     assert np.abs(dW0 - grads["W_down0"].numpy()).max() < 1e-10
+
+
+@pytest.mark.parametrize("variant", ["no_proj", "shift"])
+@pytest.mark.parametrize("name", ["H", "X0", "W_down0", "conv_w"])
+def test_variant_gradients_match_central_differences(variant, name):
+    """The ablation variants (identity projection; conv window ending at the next token) against
+    finite differences of the numpy oracle's own variant forward."""
+    w, x, dO, dWf = _case(T=19)
+    shift = 1 if variant == "shift" else 0
+    if variant == "no_proj":
+        x["W_target"] = None
+    grads = layer_backward(*(x[n] for n in NAMES), w.C, w.eta, dO, dWf, shift=shift)
+    assert (grads["W_target"] is None) == (variant == "no_proj")
+    v = torch.randn(x[name].shape, generator=torch.Generator().manual_seed(7), dtype=torch.float64)
+
+    def loss(xx):
+        O, Wf = oracle.layer_forward(*(xx[n] for n in NAMES), w.C, w.eta, shift=shift)
+        return float((O * dO.numpy()).sum() + (Wf * dWf.numpy()).sum())
+
+    h = 1e-5
+    xp, xm = dict(x), dict(x)
+    xp[name] = x[name] + h * v
+    xm[name] = x[name] - h * v
+    fd = (loss(xp) - loss(xm)) / (2 * h)
+    an = float((grads[name] * v).sum())
+    assert abs(fd - an) <= 1e-6 * max(1.0, abs(an))
+
+
+def test_shifted_conv_adjoint_by_brute_force():
+    """dX0 of the shifted variant is the transpose of the shifted conv, built as an explicit
+    [T, T] matrix per channel, applied to the gradient that reaches V (identity projection)."""
+    w, x, dO, _ = _case(B=1, T=11, d=3, f=4, C=4, k=3)
+    x["W_target"] = None
+    grads = layer_backward(*(x[n] for n in NAMES), w.C, w.eta, dO, None, shift=1)
+    k, T = w.k, w.T
+    cw = x["conv_w"]
+    # the gradient w.r.t. V, from the chunk loop written with V as the free variable
+    V = torch.zeros(T, w.d, dtype=torch.float64, requires_grad=True)
+    A = x["H"][0] @ x["W_gate"].T
+    Z = A * torch.sigmoid(A) * (x["H"][0] @ x["W_up"].T)
+    W = x["W_down0"]
+    outs = []
+    for lo in range(0, T, w.C):
+        hi = min(lo + w.C, T)
+        outs.append(Z[lo:hi] @ W.T)
+        W = W + w.eta * (V[lo:hi].T @ Z[lo:hi])
+    (torch.cat(outs) * dO[0]).sum().backward()
+    dV = V.grad.numpy()
+    for c in range(w.d):
+        M = np.zeros((T, T))  # Y[:, c] = M X0[:, c]
+        for t in range(T):
+            for s in range(k):
+                src = t + 1 - (k - 1) + s
+                if 0 <= src < T:
+                    M[t, src] = cw[c, s].item()
+        assert np.abs(M.T @ dV[:, c] - grads["X0"][0, :, c].numpy()).max() < 1e-10

@@ -231,6 +231,15 @@ bool map_3d(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int
   return encode_map(ctx, m, base, 3, dims, strides, box);
 }
 
+// [outer, mid, inner] bf16 whose rows are row_stride elements apart (inner <= row_stride).
+bool map_3d_strided(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int64_t mid, int64_t inner,
+                    int64_t row_stride, uint32_t box_mid) {
+  const uint64_t dims[3] = {(uint64_t)inner, (uint64_t)mid, (uint64_t)outer};
+  const uint64_t strides[2] = {(uint64_t)row_stride * 2, (uint64_t)row_stride * mid * 2};
+  const uint32_t box[3] = {64, box_mid, 1};
+  return encode_map(ctx, m, base, 3, dims, strides, box);
+}
+
 // [outer, mid, inner] fp32 row-major, box = 32 inner (128 bytes) x box_mid x 1.
 bool map_3d_f32(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int64_t mid, int64_t inner,
                 uint32_t box_mid) {
@@ -252,6 +261,12 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
   e = cudaFuncSetAttribute(gemm::tc_gemm_kernel<gemm::kApply>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            gemm::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (apply)");
+  e = cudaFuncSetAttribute(gemm::tc_gemm_kernel<gemm::kSwigluSave>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           gemm::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (swiglu save)");
+  e = cudaFuncSetAttribute(gemm::tc_gemm_kernel<gemm::kTwoSeg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           gemm::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (two-segment)");
   e = cudaFuncSetAttribute(state::tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            state::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (state)");
@@ -287,7 +302,7 @@ ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const voi
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
     gemm::tc_gemm_kernel<gemm::kSwiglu><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb0, mb1, mo,
-                                                                                                    p);
+                                                                                                    mo, p);
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(H);
@@ -357,7 +372,8 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
     p.st = dev_status(ctx);
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-    gemm::tc_gemm_kernel<gemm::kTarget><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, mo, p);
+    gemm::tc_gemm_kernel<gemm::kTarget><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, mo, mo,
+                                                                                                    p);
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(Y);
@@ -427,13 +443,13 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
   const int64_t df = d * f;
   dim3 g2(ceil_div(df, 256), (unsigned)B);
   simt::chunk_scan_f32_kernel<<<g2, 256, 0, ctx->stream>>>(static_cast<float*>(W_eff), static_cast<const float*>(W0),
-                                                             W_final, (int)B, (int)n, df, W_init);
+                                                             W_final, (int)B, (int)n, df, W_init, 0);
   return check_launch(ctx, "scan launch");
 }
 
 // W0 (bf16, optional): chunk 0 of every sequence is applied with W0 instead of W_eff[b, 0].
 ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t B, int64_t T, int64_t d, int64_t f,
-                       int64_t C, ipttt_dtype dt, void* O, const void* W0 = nullptr) {
+                       int64_t C, ipttt_dtype dt, void* O, const void* W0 = nullptr, float scale = 1.f) {
   const int64_t n = n_chunks_of(T, C);
   if (B == 0 || n == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
@@ -452,13 +468,14 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
     p.k_blocks = ceil_div(f, gemm::BK);
     p.problems = (int)(B * n);
     p.group_m = 16;
-    p.scale = 1.f;
+    p.scale = scale;
     p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
     p.first_from_w0 = W0 != nullptr ? 1 : 0;
     p.st = dev_status(ctx);
     const int tiles = p.problems * p.m_tiles * p.n_tiles;
     const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-    gemm::tc_gemm_kernel<gemm::kApply><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mw0, mo, p);
+    gemm::tc_gemm_kernel<gemm::kApply><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mw0, mo, mo,
+                                                                                                   p);
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(Z);
@@ -472,7 +489,7 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
     p.a_z = 0, p.b_z = d * f, p.c_z = 0;
     p.chunked = 1;
     p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
-    p.scale = 1.f;
+    p.scale = scale;
     dim3 grid(ceil_div(d, simt::SG_BN), ceil_div(C, simt::SG_BM), (unsigned)(B * n));
     simt::sgemm_kernel<false><<<grid, 256, 0, ctx->stream>>>(p);
   }
@@ -536,6 +553,298 @@ ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z,
       cudaLaunchKernelEx(&cfg, fused::tc_state_apply_kernel, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "state+apply launch");
   return check_launch(ctx, "state+apply launch");
+}
+
+// ------------------------------------------------------------------ backward pass
+
+// One state-kernel launch in its general form (bf16): accumulator rows are the M columns of the
+// token-major A operand (rows of V apart by v_stride elements), accumulator columns the N
+// columns of Z (apart by z_stride); start from W_init (fp32), W0 (bf16) or zero; chunks in
+// order or reversed; snapshots (bf16) into W_eff unless skip_first with one chunk.
+ipttt_status launch_state_general(ipttt_ctx* ctx, const void* V, int64_t v_stride, const void* Z, int64_t z_stride,
+                                  int64_t B, int64_t T, int64_t M, int64_t N, int64_t C, const void* W0,
+                                  const float* W_init, bool skip_first, bool reverse, void* W_eff, float* W_final) {
+  const int64_t n = n_chunks_of(T, C);
+  CUtensorMap mv, mz, mw, mf;
+  if (!map_3d_strided(ctx, &mv, V, B, T, M, v_stride, 64) || !map_3d_strided(ctx, &mz, Z, B, T, N, z_stride, 64) ||
+      !map_3d_f32(ctx, &mf, W_final, B, M, N, 32))
+    return IPTTT_ERR_CUDA;
+  if (W_eff != nullptr) {
+    if (!map_3d(ctx, &mw, W_eff, B * n, M, N, 32)) return IPTTT_ERR_CUDA;
+  } else {
+    mw = mv;  // never stored through: one chunk and no first snapshot
+  }
+  state::Params p{};
+  p.B = (int)B;
+  p.T = (int)T;
+  p.d = (int)M;
+  p.f = (int)N;
+  p.C = (int)C;
+  p.n_chunks = (int)n;
+  p.m_units = ceil_div(M, state::BMD);
+  p.n_units = ceil_div(N, state::BNF);
+  p.units = (int)(B * p.m_units * p.n_units);
+  p.W0 = static_cast<const __nv_bfloat16*>(W0);
+  p.skip_first = skip_first ? 1 : 0;
+  p.W_init = W_init;
+  p.reverse = reverse ? 1 : 0;
+  p.st = dev_status(ctx);
+  const int pairs = (p.units + 1) / 2;
+  const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
+  state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, mw, mf, p);
+  return check_launch(ctx, "state launch");
+}
+
+// C = A1 B1 + A2 B2 (bf16, kTwoSeg): A segments token-major [B, T, K] (a2 = A1's map shifted by
+// a2_koff columns when a2 is NULL), B segments [slices, K, N]; per chunk when b_per_problem.
+ipttt_status launch_two_seg(ipttt_ctx* ctx, const void* A1, int64_t a1_stride, const void* A2, int64_t a2_stride,
+                            int64_t a2_koff, const void* B1, const void* B2, int64_t b_slices, bool b_per_problem,
+                            int64_t B, int64_t T, int64_t C, int64_t K1, int64_t K2, int64_t N, void* out) {
+  const int64_t n = n_chunks_of(T, C);
+  CUtensorMap ma1, ma2, mb1, mb2, mo;
+  // segment 1 is cut at K1 columns (its ragged K block reads zeros, not segment 2); without its
+  // own pointer segment 2 is read through a map over [A1 | A2] at column offset a2_koff
+  const bool shared = A2 == nullptr;
+  if (!map_3d_strided(ctx, &ma1, A1, B, T, K1, a1_stride, 128) ||
+      !map_3d_strided(ctx, &ma2, shared ? A1 : A2, B, T, shared ? a2_koff + K2 : K2, shared ? a1_stride : a2_stride,
+                      128) ||
+      !map_3d(ctx, &mb1, B1, b_slices, K1, N, 64) || !map_3d(ctx, &mb2, B2, b_slices, K2, N, 64) ||
+      !map_3d(ctx, &mo, out, B, T, N, 32))
+    return IPTTT_ERR_CUDA;
+  gemm::Params p{};
+  p.m_tiles = (int)(C / gemm::BM);
+  p.n_tiles = ceil_div(N, gemm::BN);
+  p.k_blocks = ceil_div(K1, gemm::BK);
+  p.k_blocks2 = ceil_div(K2, gemm::BK);
+  p.a2_koff = shared ? (int)a2_koff : 0;
+  p.b_per_problem = b_per_problem ? 1 : 0;
+  p.problems = (int)(B * n);
+  p.group_m = 16;
+  p.scale = 1.f;
+  p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
+  p.st = dev_status(ctx);
+  const int tiles = p.problems * p.m_tiles * p.n_tiles;
+  const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+  gemm::tc_gemm_kernel<gemm::kTwoSeg><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma1, mb1, ma2, mo,
+                                                                                                    mb2, p);
+  return check_launch(ctx, "two-segment launch");
+}
+
+// fp32 CUDA-core GEMM helper: C[z] = scale * A B (+ beta C) with element strides.
+ipttt_status sgemm(ipttt_ctx* ctx, const float* A, int64_t a_sm, int64_t a_sk, const float* Bm, int64_t b_sk,
+                   int64_t b_sn, float* Cm, int64_t c_sm, int64_t M, int64_t N, int64_t K, float scale, float beta,
+                   int chunked = 0, int64_t T = 0, int64_t C = 0, int64_t n = 0, int64_t Bseq = 1, int64_t a_tok = 0,
+                   int64_t b_tok = 0, int64_t c_tok = 0, int64_t a_z = 0, int64_t b_z = 0, int64_t c_z = 0) {
+  simt::SgemmParams p{};
+  p.A = A, p.B = Bm, p.Cm = Cm;
+  p.M = (int)M, p.N = (int)N, p.K = (int)K;
+  p.a_sm = a_sm, p.a_sk = a_sk, p.b_sk = b_sk, p.b_sn = b_sn, p.c_sm = c_sm;
+  p.a_tok = a_tok, p.b_tok = b_tok, p.c_tok = c_tok, p.a_z = a_z, p.b_z = b_z, p.c_z = c_z;
+  p.chunked = chunked;
+  p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
+  p.scale = scale;
+  p.beta = beta;
+  dim3 grid(ceil_div(N, simt::SG_BN), ceil_div(M, simt::SG_BM), (unsigned)(chunked ? Bseq * n : 1));
+  simt::sgemm_kernel<false><<<grid, 256, 0, ctx->stream>>>(p);
+  return check_launch(ctx, "sgemm launch");
+}
+
+struct BwdLayout {
+  size_t y, v, z, au, dz, dv, dy, wst, rst, dw0b, part, total;
+  int64_t strips;
+};
+
+BwdLayout bwd_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, int k, ipttt_dtype dt) {
+  const size_t es = esize(dt);
+  const int64_t n = n_chunks_of(T, C);
+  BwdLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  L.y = take((size_t)B * T * d * es);
+  L.v = take((size_t)B * T * d * es);
+  L.z = take((size_t)B * T * f * es);
+  L.au = take((size_t)B * T * 2 * f * es);
+  L.dz = take((size_t)B * T * f * es);
+  L.dv = take((size_t)B * T * d * es);
+  L.dy = take((size_t)B * T * d * es);
+  L.wst = take((size_t)B * n * d * f * es);
+  L.rst = take((size_t)B * n * d * f * es);
+  L.dw0b = take((size_t)B * d * f * 4);
+  L.strips = B * ((T + simt::CONVW_STRIP - 1) / simt::CONVW_STRIP);
+  L.part = take((size_t)L.strips * d * k * 4);
+  L.total = off;
+  return L;
+}
+
+// The backward pass (validated by the caller; T >= 1).
+ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
+                          const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d, int64_t f,
+                          int64_t C, int k, float eta, ipttt_dtype dt, const void* dO, const float* dW_final,
+                          void* dH, void* dX0, float* dWg, float* dWu, float* dW0, float* dWt, float* dcw, void* ws) {
+  ipttt_status s = IPTTT_OK;
+  const BwdLayout L = bwd_layout(B, T, d, f, C, k, dt);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* Y = base + L.y;
+  void* V = base + L.v;
+  void* Z = base + L.z;
+  void* AU = base + L.au;
+  void* dZ = base + L.dz;
+  void* dV = base + L.dv;
+  void* dY = base + L.dy;
+  void* Wst = base + L.wst;
+  void* Rst = base + L.rst;
+  float* dW0b = reinterpret_cast<float*>(base + L.dw0b);
+  float* part = reinterpret_cast<float*>(base + L.part);
+  const int64_t n = n_chunks_of(T, C);
+  const int64_t BT = B * T;
+  const int64_t CT = (BT + 127) / 128 * 128;  // all tokens as one chunk (flat GEMMs and reductions)
+  const bool bf16 = dt == IPTTT_BF16;
+  const int64_t df = d * f;
+  if (bf16) {
+    if ((s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+    // forward recompute: Z and the pre-activations [A | U]
+    {
+      // [A | U] as [rows][2][d_ff]: a box never crosses from the gate half into the up half
+      CUtensorMap ma, mb0, mb1, mo, mx;
+      const uint64_t au_dims[3] = {(uint64_t)f, 2, (uint64_t)BT};
+      const uint64_t au_strides[2] = {(uint64_t)f * 2, (uint64_t)f * 4};
+      const uint32_t au_box[3] = {64, 1, 32};
+      if (!map_2d(ctx, &ma, H, BT, d, 64, 128) || !map_2d(ctx, &mb0, Wg, f, d, 64, 128) ||
+          !map_2d(ctx, &mb1, Wu, f, d, 64, 128) || !map_2d(ctx, &mo, Z, BT, f, 64, 32) ||
+          !encode_map(ctx, &mx, AU, 3, au_dims, au_strides, au_box))
+        return IPTTT_ERR_CUDA;
+      gemm::Params p{};
+      p.m_tiles = ceil_div(BT, gemm::BM);
+      p.n_tiles = ceil_div(f, 128);
+      p.k_blocks = ceil_div(d, gemm::BK);
+      p.problems = 1;
+      p.group_m = 16;
+      p.scale = 1.f;
+      p.st = dev_status(ctx);
+      const int tiles = p.m_tiles * p.n_tiles;
+      const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+      gemm::tc_gemm_kernel<gemm::kSwigluSave><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(
+          ma, mb0, mb1, mo, mx, p);
+      if ((s = check_launch(ctx, "swiglu save launch")) != IPTTT_OK) return s;
+    }
+  } else {
+    // A -> AU[:, :f], U -> AU[:, f:], then Z = SiLU(A) U
+    float* au = static_cast<float*>(AU);
+    if ((s = sgemm(ctx, static_cast<const float*>(H), d, 1, static_cast<const float*>(Wg), 1, d, au, 2 * f, BT, f, d,
+                   1.f, 0.f)) != IPTTT_OK ||
+        (s = sgemm(ctx, static_cast<const float*>(H), d, 1, static_cast<const float*>(Wu), 1, d, au + f, 2 * f, BT, f,
+                   d, 1.f, 0.f)) != IPTTT_OK)
+      return s;
+    simt::swiglu_combine_kernel<float><<<ceil_div(BT * f, 256), 256, 0, ctx->stream>>>(au, static_cast<float*>(Z),
+                                                                                       BT, (int)f);
+    if ((s = check_launch(ctx, "combine launch")) != IPTTT_OK) return s;
+  }
+  // target and forward weights of every chunk (the forward's W_final goes to scratch)
+  if (Wt != nullptr) {
+    if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, Y)) != IPTTT_OK) return s;
+    if ((s = run_target_gemm(ctx, Y, Wt, BT, d, eta, dt, V)) != IPTTT_OK) return s;
+  } else if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, V, nullptr, eta)) != IPTTT_OK) {  // V = eta * conv(X0)
+    return s;
+  }
+  if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, dW0b, false)) != IPTTT_OK) return s;
+  if (bf16) {
+    // reverse scan: R_i = dW_final + sum_{l>i} dO_l^T Z_l, final = dW_final + sum_i dO_i^T Z_i
+    if ((s = launch_state_general(ctx, dO, d, Z, f, B, T, d, f, C, nullptr, dW_final, false, true, Rst, dW0b)) !=
+        IPTTT_OK)
+      return s;
+    // dZ_i = dO_i W_i + V_i R_i (V carries eta)
+    if ((s = launch_two_seg(ctx, dO, d, V, d, 0, Wst, Rst, B * n, true, B, T, C, d, d, f, dZ)) != IPTTT_OK) return s;
+  } else {
+    float* rst = static_cast<float*>(Rst);
+    // G_i = dO_i^T Z_i per chunk, then the reverse exclusive scan
+    if ((s = sgemm(ctx, static_cast<const float*>(dO), 1, d, static_cast<const float*>(Z), f, 1, rst, f, d, f, C, 1.f,
+                   0.f, 2, T, C, n, B, d, f, 0, 0, 0, df)) != IPTTT_OK)
+      return s;
+    dim3 g2(ceil_div(df, 256), (unsigned)B);
+    simt::chunk_scan_f32_kernel<<<g2, 256, 0, ctx->stream>>>(rst, nullptr, dW0b, (int)B, (int)n, df, dW_final, 1);
+    if ((s = check_launch(ctx, "reverse scan launch")) != IPTTT_OK) return s;
+    // dZ_i = dO_i W_i + V_i R_i
+    if ((s = sgemm(ctx, static_cast<const float*>(dO), d, 1, static_cast<const float*>(Wst), f, 1,
+                   static_cast<float*>(dZ), f, C, f, d, 1.f, 0.f, 1, T, C, n, B, d, 0, f, 0, df, 0)) != IPTTT_OK ||
+        (s = sgemm(ctx, static_cast<const float*>(V), d, 1, rst, f, 1, static_cast<float*>(dZ), f, C, f, d, 1.f, 1.f,
+                   1, T, C, n, B, d, 0, f, 0, df, 0)) != IPTTT_OK)
+      return s;
+  }
+  // gated-MLP backward in place: AU -> [dA | dU]
+  if (bf16)
+    simt::swiglu_backward_kernel<__nv_bfloat16><<<ceil_div(BT * f, 256), 256, 0, ctx->stream>>>(
+        static_cast<const __nv_bfloat16*>(dZ), static_cast<__nv_bfloat16*>(AU), BT, (int)f);
+  else
+    simt::swiglu_backward_kernel<float><<<ceil_div(BT * f, 256), 256, 0, ctx->stream>>>(
+        static_cast<const float*>(dZ), static_cast<float*>(AU), BT, (int)f);
+  if ((s = check_launch(ctx, "swiglu backward launch")) != IPTTT_OK) return s;
+  if (bf16) {
+    const size_t es = 2;
+    // dH = dA W_gate + dU W_up
+    if ((s = launch_two_seg(ctx, AU, 2 * f, nullptr, 2 * f, f, Wg, Wu, 1, false, 1, BT, CT, f, f, d, dH)) != IPTTT_OK)
+      return s;
+    // dW_gate = dA^T H, dW_up = dU^T H (reductions over all tokens)
+    if ((s = launch_state_general(ctx, AU, 2 * f, H, d, 1, BT, f, d, CT, nullptr, nullptr, true, false, nullptr,
+                                  dWg)) != IPTTT_OK ||
+        (s = launch_state_general(ctx, static_cast<uint8_t*>(AU) + f * es, 2 * f, H, d, 1, BT, f, d, CT, nullptr,
+                                  nullptr, true, false, nullptr, dWu)) != IPTTT_OK)
+      return s;
+  } else {
+    const float* au = static_cast<const float*>(AU);
+    if ((s = sgemm(ctx, au, 2 * f, 1, static_cast<const float*>(Wg), d, 1, static_cast<float*>(dH), d, BT, d, f, 1.f,
+                   0.f)) != IPTTT_OK ||
+        (s = sgemm(ctx, au + f, 2 * f, 1, static_cast<const float*>(Wu), d, 1, static_cast<float*>(dH), d, BT, d, f,
+                   1.f, 1.f)) != IPTTT_OK ||
+        (s = sgemm(ctx, au, 1, 2 * f, static_cast<const float*>(H), d, 1, dWg, d, f, d, BT, 1.f, 0.f)) != IPTTT_OK ||
+        (s = sgemm(ctx, au + f, 1, 2 * f, static_cast<const float*>(H), d, 1, dWu, d, f, d, BT, 1.f, 0.f)) != IPTTT_OK)
+      return s;
+  }
+  // dV = eta Z R^T (per chunk), dY = dV W_target^T, dW_target = Y^T dV (without a projection
+  // dY is dV itself)
+  if ((s = run_apply(ctx, Z, Rst, B, T, d, f, C, dt, dV, nullptr, eta)) != IPTTT_OK) return s;
+  if (Wt == nullptr) {
+    dY = dV;
+  } else if (bf16) {
+    if ((s = run_apply(ctx, dV, Wt, 1, BT, d, d, CT, dt, dY)) != IPTTT_OK) return s;
+    if ((s = launch_state_general(ctx, Y, d, dV, d, 1, BT, d, d, CT, nullptr, nullptr, true, false, nullptr, dWt)) !=
+        IPTTT_OK)
+      return s;
+  } else {
+    if ((s = sgemm(ctx, static_cast<const float*>(dV), d, 1, static_cast<const float*>(Wt), 1, d,
+                   static_cast<float*>(dY), d, BT, d, d, 1.f, 0.f)) != IPTTT_OK ||
+        (s = sgemm(ctx, static_cast<const float*>(Y), 1, d, static_cast<const float*>(dV), d, 1, dWt, d, d, d, BT, 1.f,
+                   0.f)) != IPTTT_OK)
+      return s;
+  }
+  // the causal conv's adjoints
+  {
+    const int64_t nx = BT * d;
+    dim3 gw(ceil_div(d, 128), (unsigned)L.strips);
+    if (bf16) {
+      simt::conv_backward_x_kernel<__nv_bfloat16><<<ceil_div(nx, 256), 256, 0, ctx->stream>>>(
+          static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(cw), static_cast<__nv_bfloat16*>(dX0),
+          (int)B, (int)T, (int)d, k, ctx->target_shift);
+      simt::conv_backward_w_partial_kernel<__nv_bfloat16><<<gw, 128, 0, ctx->stream>>>(
+          static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(X0), part, (int)B, (int)T, (int)d, k,
+          ctx->target_shift);
+    } else {
+      simt::conv_backward_x_kernel<float><<<ceil_div(nx, 256), 256, 0, ctx->stream>>>(
+          static_cast<const float*>(dY), static_cast<const float*>(cw), static_cast<float*>(dX0), (int)B, (int)T,
+          (int)d, k, ctx->target_shift);
+      simt::conv_backward_w_partial_kernel<float><<<gw, 128, 0, ctx->stream>>>(
+          static_cast<const float*>(dY), static_cast<const float*>(X0), part, (int)B, (int)T, (int)d, k,
+          ctx->target_shift);
+    }
+    simt::sum_strips_kernel<<<ceil_div(d * k, 256), 256, 0, ctx->stream>>>(part, dcw, (int)L.strips, d * k);
+    if ((s = check_launch(ctx, "conv backward launch")) != IPTTT_OK) return s;
+  }
+  // the shared initial fast weight: sum over sequences
+  simt::sum_strips_kernel<<<ceil_div(df, 256), 256, 0, ctx->stream>>>(dW0b, dW0, (int)B, df);
+  return check_launch(ctx, "batch sum launch");
 }
 
 void mark(ipttt_ctx* ctx, int call, int which, cudaStream_t stream) {
@@ -884,6 +1193,105 @@ ipttt_status ipttt_layer_forward(ipttt_ctx* ctx, const void* H, const void* X0, 
   if (s != IPTTT_OK) return s;
   DeviceGuard g(ctx->device);
   return run_layer(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, O, W_final, ws);
+}
+
+ipttt_status ipttt_backward_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
+                                           ipttt_dtype dt, size_t* bytes) {
+  if (!bytes) return IPTTT_ERR_INVALID_ARG;
+  const ipttt_status s = check_shape(nullptr, B, T, d, d_ff, C, k, dt);
+  if (s != IPTTT_OK) return s;
+  *bytes = bwd_layout(B, T, d, d_ff, C, k, dt).total;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                  const void* W_up, const void* W_down0, const void* W_target, const void* conv_w,
+                                  int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k, float eta,
+                                  ipttt_dtype dt, const void* dO, const float* dW_final, void* dH, void* dX0,
+                                  float* dW_gate, float* dW_up, float* dW_down0, float* dW_target, float* dconv_w,
+                                  void* ws, size_t ws_bytes) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, B, T, d, d_ff, C, k, dt);
+  if (s != IPTTT_OK) return s;
+  if (!std::isfinite(eta)) {
+    set_err(ctx, "eta is not finite");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (B * T >= (int64_t)1 << 31) {
+    set_err(ctx, "B*T must be < 2^31");
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  if (B > 65535 || B * ((T + simt::CONVW_STRIP - 1) / simt::CONVW_STRIP) > 65535) {
+    set_err(ctx, "B (%lld) and B*ceil(T/%d) must be <= 65535", (long long)B, simt::CONVW_STRIP);
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  const bool work = B > 0 && T > 0;
+  struct P {
+    const void* p;
+    const char* n;
+    bool needed;
+  } ptrs[] = {{H, "H", work},         {X0, "X0", work},         {W_gate, "W_gate", work}, {W_up, "W_up", work},
+              {W_down0, "W_down0", work}, {conv_w, "conv_w", work}, {dO, "dO", work},       {dH, "dH", work},
+              {dX0, "dX0", work},     {dW_gate, "dW_gate", true}, {dW_up, "dW_up", true}, {dW_down0, "dW_down0", true},
+              {dconv_w, "dconv_w", true}, {ws, "workspace", work}, {W_target, "W_target", false},
+              {dW_target, "dW_target", W_target != nullptr}, {dW_final, "dW_final", false}};
+  for (const P& q : ptrs) {
+    if (q.needed && !q.p) {
+      set_err(ctx, "%s is NULL", q.n);
+      return IPTTT_ERR_INVALID_ARG;
+    }
+    if (q.p && !aligned16(q.p)) {
+      set_err(ctx, "%s is not 16-byte aligned", q.n);
+      return IPTTT_ERR_INVALID_ARG;
+    }
+  }
+  const BwdLayout L = bwd_layout(B, T, d, d_ff, C, k, dt);
+  if (work && ws_bytes < L.total) {
+    set_err(ctx, "workspace too small: %zu < %zu bytes", ws_bytes, L.total);
+    return IPTTT_ERR_WORKSPACE;
+  }
+  const size_t es = esize(dt);
+  const size_t act = (size_t)B * T * d * es, wdf = (size_t)d * d_ff * es, gdf = (size_t)d * d_ff * 4;
+  std::vector<Region> all = {{H, act, "H"},
+                             {X0, act, "X0"},
+                             {W_gate, wdf, "W_gate"},
+                             {W_up, wdf, "W_up"},
+                             {W_down0, wdf, "W_down0"},
+                             {W_target, (size_t)d * d * es, "W_target"},
+                             {conv_w, (size_t)d * k * es, "conv_w"},
+                             {dO, act, "dO"},
+                             {dW_final, (size_t)B * gdf, "dW_final"},
+                             {dH, act, "dH"},
+                             {dX0, act, "dX0"},
+                             {dW_gate, gdf, "dW_gate"},
+                             {dW_up, gdf, "dW_up"},
+                             {dW_down0, gdf, "dW_down0"},
+                             {dW_target, W_target ? (size_t)d * d * 4 : 0, "dW_target"},
+                             {dconv_w, (size_t)d * k * 4, "dconv_w"},
+                             {ws, work ? L.total : 0, "workspace"}};
+  std::vector<Region> outs(all.begin() + 9, all.end());
+  std::string what;
+  if (find_overlap(outs, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  if (!work) {
+    // no tokens: every gradient is zero except dW_down0 = sum_b dW_final[b]
+    cudaMemsetAsync(dW_gate, 0, gdf, ctx->stream);
+    cudaMemsetAsync(dW_up, 0, gdf, ctx->stream);
+    if (dW_target) cudaMemsetAsync(dW_target, 0, (size_t)d * d * 4, ctx->stream);
+    cudaMemsetAsync(dconv_w, 0, (size_t)d * k * 4, ctx->stream);
+    if (dW_final != nullptr && B > 0) {
+      simt::sum_strips_kernel<<<ceil_div(d * d_ff, 256), 256, 0, ctx->stream>>>(dW_final, dW_down0, (int)B,
+                                                                                 d * d_ff);
+    } else {
+      cudaMemsetAsync(dW_down0, 0, gdf, ctx->stream);
+    }
+    return check_launch(ctx, "empty backward");
+  }
+  return run_backward(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, dO, dW_final,
+                      dH, dX0, dW_gate, dW_up, dW_down0, dW_target, dconv_w, ws);
 }
 
 ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,

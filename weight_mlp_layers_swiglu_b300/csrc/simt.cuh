@@ -146,6 +146,7 @@ struct SgemmParams {
   int chunked;                  // 0: plain; 1: chunk length is M; 2: chunk length is K
   int T, C, n_chunks;
   float scale;
+  float beta;  // C = scale * A B + beta * C (beta = 0: C is only written)
 };
 
 constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16;
@@ -227,6 +228,7 @@ __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmParams p) {
       } else {
         v = acc[i][j] * p.scale;
       }
+      if (p.beta != 0.f) v += p.beta * Cm[gm * p.c_sm + gn];
       Cm[gm * p.c_sm + gn] = v;
     }
   }
@@ -235,21 +237,113 @@ __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmParams p) {
 // --------------------------------------------------------------------------- exclusive scan
 // In place over the stack: on entry W[b, i] holds Delta_i (already scaled by eta); on exit
 // W[b, i] = W0 + sum_{j<i} Delta_j and W_final[b] = W0 + sum_j Delta_j.
-// W_init (optional, [B, d, d_ff]): each sequence's own starting state instead of W0.
+// W_init (optional, [B, d, d_ff]): each sequence's own starting state instead of W0 (W0 NULL
+// too: zero).  reverse = 1 scans the chunks last to first (exclusive suffix sums).
 __global__ void chunk_scan_f32_kernel(float* __restrict__ W, const float* __restrict__ W0,
                                       float* __restrict__ W_final, int B, int n_chunks, int64_t df,
-                                      const float* __restrict__ W_init) {
+                                      const float* __restrict__ W_init, int reverse) {
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int b = blockIdx.y;
   if (e >= df) return;
-  float acc = W_init != nullptr ? W_init[(int64_t)b * df + e] : W0[e];
+  float acc = W_init != nullptr ? W_init[(int64_t)b * df + e] : (W0 != nullptr ? W0[e] : 0.f);
   float* w = W + (int64_t)b * n_chunks * df + e;
-  for (int i = 0; i < n_chunks; ++i) {
+  for (int j = 0; j < n_chunks; ++j) {
+    const int i = reverse ? n_chunks - 1 - j : j;
     const float delta = w[(int64_t)i * df];
     w[(int64_t)i * df] = acc;
     acc += delta;
   }
   W_final[(int64_t)b * df + e] = acc;
+}
+
+// ------------------------------------------------------------------ backward-pass helpers
+
+template <typename T>
+__device__ __forceinline__ float ld_f(const T* p) { return static_cast<float>(*p); }
+template <typename T>
+__device__ __forceinline__ void st_f(T* p, float v) { *p = static_cast<T>(v); }
+
+// Z = SiLU(A) * U from the saved pre-activations AU = [A | U] ([rows, 2f]).
+template <typename T>
+__global__ void swiglu_combine_kernel(const T* __restrict__ AU, T* __restrict__ Z, int64_t rows, int f) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= rows * f) return;
+  const int64_t r = e / f;
+  const int j = (int)(e % f);
+  const float a = ld_f(AU + r * 2 * f + j), u = ld_f(AU + r * 2 * f + f + j);
+  st_f(Z + e, a / (1.0f + expf(-a)) * u);
+}
+
+// Gated-MLP backward, in place: AU = [A | U] becomes [dA | dU] with
+// dA = dZ * U * s * (1 + A (1 - s)), s = sigmoid(A), and dU = dZ * A * s (the derivative of
+// SiLU(a) = a * sigmoid(a) is s (1 + a (1 - s))).
+template <typename T>
+__global__ void swiglu_backward_kernel(const T* __restrict__ dZ, T* __restrict__ AU, int64_t rows, int f) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= rows * f) return;
+  const int64_t r = e / f;
+  const int j = (int)(e % f);
+  T* pa = AU + r * 2 * f + j;
+  T* pu = pa + f;
+  const float a = ld_f(pa), u = ld_f(pu), dz = ld_f(dZ + e);
+  const float sg = 1.0f / (1.0f + expf(-a));
+  st_f(pa, dz * u * sg * (1.0f + a * (1.0f - sg)));
+  st_f(pu, dz * a * sg);
+}
+
+// Adjoint of the causal depthwise conv for its input: with the window shifted by `shift` tokens,
+// dX0[u, c] = sum_s w[c, s] dY[u - shift + (k-1) - s, c] over the rows that exist.
+template <typename T>
+__global__ void conv_backward_x_kernel(const T* __restrict__ dY, const T* __restrict__ conv_w, T* __restrict__ dX0,
+                                       int B, int T_len, int d, int k, int shift) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t n = (int64_t)B * T_len * d;
+  if (e >= n) return;
+  const int c = (int)(e % d);
+  const int64_t bt = e / d;
+  const int t = (int)(bt % T_len);
+  const int64_t base = bt - t;  // b * T_len
+  float acc = 0.f;
+  for (int s = 0; s < k; ++s) {
+    const int src = t - shift + (k - 1) - s;
+    if (src >= 0 && src < T_len) acc = fmaf(static_cast<float>(conv_w[(int64_t)c * k + s]), ld_f(dY + (base + src) * d + c), acc);
+  }
+  st_f(dX0 + e, acc);
+}
+
+// Adjoint for the taps, in two passes (deterministic): partial[strip, c, s] = sum over the strip's
+// tokens of dY[t, c] X0[t + shift - (k-1) + s, c]; then dconv_w[c, s] = sum over strips in order.
+constexpr int CONVW_STRIP = 256;
+
+template <typename T>
+__global__ void conv_backward_w_partial_kernel(const T* __restrict__ dY, const T* __restrict__ X0,
+                                               float* __restrict__ partial, int B, int T_len, int d, int k,
+                                               int shift) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int strip = blockIdx.y;  // over B * ceil(T / CONVW_STRIP)
+  const int per_b = (T_len + CONVW_STRIP - 1) / CONVW_STRIP;
+  if (c >= d) return;
+  const int b = strip / per_b;
+  const int t0 = (strip % per_b) * CONVW_STRIP;
+  const int t1 = min(t0 + CONVW_STRIP, T_len);
+  const T* dy = dY + (int64_t)b * T_len * d + c;
+  const T* x = X0 + (int64_t)b * T_len * d + c;
+  for (int s = 0; s < k; ++s) {
+    float acc = 0.f;
+    for (int t = t0; t < t1; ++t) {
+      const int src = t + shift - (k - 1) + s;
+      if (src >= 0 && src < T_len) acc = fmaf(ld_f(dy + (int64_t)t * d), ld_f(x + (int64_t)src * d), acc);
+    }
+    partial[((int64_t)strip * d + c) * k + s] = acc;
+  }
+}
+
+__global__ void sum_strips_kernel(const float* __restrict__ partial, float* __restrict__ out, int strips, int64_t n) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  float acc = 0.f;
+  for (int i = 0; i < strips; ++i) acc += partial[(int64_t)i * n + e];
+  out[e] = acc;
 }
 
 // W_final[b] = W0 (as fp32) for every sequence: the state of an empty sequence.  (A resumed

@@ -41,7 +41,10 @@ constexpr int BAR_BYTES = 256;
 constexpr int OUT_BYTES = 4 * 2 * OUT_BOX_BYTES;  // two staging boxes per epilogue warp
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + BAR_BYTES;
 
-enum Kind : int { kSwiglu = 0, kTarget = 1, kApply = 2 };
+// kSwigluSave: kSwiglu that also writes the gate and up pre-activations (for the backward pass).
+// kTwoSeg: C = A1 B1 + A2 B2 over two K segments, B operands MN-major ([K, N] row-major), per
+// chunk like kApply (the backward pass's dZ_i = dO_i W_i + V_i R_i and dH = dA W_gate + dU W_up).
+enum Kind : int { kSwiglu = 0, kTarget = 1, kApply = 2, kSwigluSave = 3, kTwoSeg = 4 };
 
 struct Params {
   int m_tiles, n_tiles, k_blocks;  // per problem
@@ -52,6 +55,9 @@ struct Params {
   int first_from_w0;   // Apply: chunk 0 of each sequence reads W_down0 (map_b1) instead of the stack
   uint32_t* zero_ptr;  // optional: CTA 0 clears zero_count words here (counters of a later kernel)
   int zero_count;
+  int k_blocks2;       // kTwoSeg: k-blocks of the second segment (the first has k_blocks)
+  int a2_koff;         // kTwoSeg: column offset of the second segment within its A map
+  int b_per_problem;   // kTwoSeg: 1 = each problem (chunk) has its own B slice, 0 = one shared B
   DevStatus st;
 };
 
@@ -69,7 +75,7 @@ __device__ __forceinline__ void decode_tile(const Params& p, int tile, int& prob
 
 template <int KIND>
 __device__ __forceinline__ bool tile_active(const Params& p, int prob, int mt) {
-  if (KIND == kApply) {
+  if (KIND == kApply || KIND == kTwoSeg) {
     const int i = prob % p.n_chunks;
     return i * p.C + mt * BM < p.T;
   }
@@ -80,7 +86,7 @@ template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                    const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_out,
-                   const Params p) {
+                   const __grid_constant__ CUtensorMap map_x, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_stage = smem + STAGES * STAGE_BYTES;
@@ -96,6 +102,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int total_tiles = p.problems * p.m_tiles * p.n_tiles;
+  const int k_total = p.k_blocks + (KIND == kTwoSeg ? p.k_blocks2 : 0);
 
   if (p.zero_ptr != nullptr && blockIdx.x == 0)
     for (int i = threadIdx.x; i < p.zero_count; i += blockDim.x) p.zero_ptr[i] = 0u;
@@ -131,12 +138,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b0);
     if (KIND != kTarget) tma_prefetch_desc(&map_b1);
+    if (KIND == kTwoSeg) tma_prefetch_desc(&map_x);
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int prob, mt, nt;
       decode_tile(p, tile, prob, mt, nt);
       if (!tile_active<KIND>(p, prob, mt)) continue;
       bool ok = true;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
+      for (int kb = 0; kb < k_total; ++kb) {
         if (!wait_bounded(&empty[p_stage], p_phase ^ 1u, p.st, abort_flag, 0x101)) {
           ok = false;
           break;
@@ -145,10 +153,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t* sb = sa + A_BYTES;
         mbar_arrive_expect_tx(&full[p_stage], STAGE_BYTES);
         const int k0 = kb * BK;
-        if (KIND == kSwiglu) {
+        if (KIND == kSwiglu || KIND == kSwigluSave) {
           tma_load_2d(sa, &map_a, &full[p_stage], k0, mt * BM);
           tma_load_2d(sb, &map_b0, &full[p_stage], k0, nt * 128);
           tma_load_2d(sb + B_BYTES / 2, &map_b1, &full[p_stage], k0, nt * 128);
+        } else if (KIND == kTwoSeg) {
+          const int b = prob / p.n_chunks;
+          const int i = prob - b * p.n_chunks;
+          const bool second = kb >= p.k_blocks;
+          const int kk0 = second ? (kb - p.k_blocks) * BK : k0;
+          const int bslice = p.b_per_problem ? prob : 0;
+          tma_load_3d(sa, second ? &map_b1 : &map_a, &full[p_stage], kk0 + (second ? p.a2_koff : 0),
+                      i * p.C + mt * BM, b);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_load_3d(sb + j * (BK * 128), second ? &map_x : &map_b0, &full[p_stage], nt * BN + j * 64, kk0,
+                        bslice);
         } else if (KIND == kTarget) {
           tma_load_2d(sa, &map_a, &full[p_stage], k0, mt * BM);
 #pragma unroll
@@ -171,7 +191,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
     }
   } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = idesc_bf16(BM, BN, false, KIND == kTarget);
+    constexpr bool b_mn = KIND == kTarget || KIND == kTwoSeg;
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, false, b_mn);
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
@@ -185,7 +206,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
       bool ok = true;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
+      for (int kb = 0; kb < k_total; ++kb) {
         if (!wait_bounded(&full[stage], phase, p.st, abort_flag, 0x103)) {
           ok = false;
           break;
@@ -196,8 +217,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint64_t adesc = sdesc_sw128(a_addr + kk * 32, 16, 1024);
-          const uint64_t bdesc = (KIND == kTarget) ? sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024)
-                                                   : sdesc_sw128(b_addr + kk * 32, 16, 1024);
+          const uint64_t bdesc = b_mn ? sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024)
+                                      : sdesc_sw128(b_addr + kk * 32, 16, 1024);
           tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[stage]);
@@ -224,7 +245,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!wait_bounded(&acc_full[buf], use & 1u, p.st, abort_flag, 0x104)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      if (KIND == kSwiglu) {
+      if (KIND == kSwiglu || KIND == kSwigluSave) {
         // 128 output columns: two boxes of 64, each from 64 gate and 64 up accumulator columns
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
@@ -245,6 +266,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           out.put(row, &map_out, nt * 128 + h * 64, mt * BM + q * 32);
+          if (KIND == kSwigluSave) {  // the gate and up pre-activations: map_x is [rows][2][d_ff]
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part) {
+              uint32_t pre[32];
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                uint32_t g[32];
+                tmem_ld32(t_row + part * 128 + h * 64 + c * 32, g);
+                tmem_ld_wait(g);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  pre[c * 16 + e] = pack_bf16x2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1]));
+              }
+              out.put(pre, &map_x, nt * 128 + h * 64, part, mt * BM + q * 32);
+            }
+          }
         }
       } else {
 #pragma unroll 1
@@ -259,7 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             row[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
             row[16 + e] = pack_bf16x2(__uint_as_float(b[2 * e]) * p.scale, __uint_as_float(b[2 * e + 1]) * p.scale);
           }
-          if (KIND == kApply) {
+          if (KIND == kApply || KIND == kTwoSeg) {
             const int bq = prob / p.n_chunks;
             const int i = prob - bq * p.n_chunks;
             out.put(row, &map_out, nt * BN + h * 64, i * p.C + mt * BM + q * 32, bq);

@@ -1,5 +1,10 @@
 // Chunk-state kernel: the running fast weight, held in tensor memory.
 //
+// The same kernel runs the backward pass's reverse scan (chunks last to first, started from
+// dW_final: its snapshots are the exclusive suffix sums R_i = dW_final + sum_{l>i} dO_l^T Z_l)
+// and, with one chunk and a zero start, plain reductions over tokens (A^T B of two
+// token-major matrices, the weight gradients).
+//
 // zhichai.net "In-Place TTT：给LLM装上"临时记忆插槽"，让它边读边学", §3.2 Steps 1-2 and the
 // §3.3 update rule: for each chunk i of a sequence, Delta_i = V_i^T Z_i, and chunk i is
 // applied with W_eff[i] = W_down0 + sum_{j<i} Delta_j (V arrives pre-scaled by eta), so
@@ -43,13 +48,22 @@ struct Params {
   const __nv_bfloat16* W0;      // [d, f]; W_eff [B, n_chunks, d, f] and W_final [B, d, f] via tensor maps
   int skip_first;               // 1: W_eff[b, 0] (= W_down0) is not written (the apply reads W_down0)
   const float* W_init;          // optional [B, d, f] fp32: each sequence's own starting state
+  int reverse;                  // 1: chunks run last to first (the backward pass's suffix scan)
   DevStatus st;
 };
 
+// The chunk processed at step j: j, or n-1-j when the scan runs backwards.
+__device__ __forceinline__ int chunk_at(const Params& p, int j) { return p.reverse ? p.n_chunks - 1 - j : j; }
+
 // The accumulator's starting value for state rows `row`, columns col .. col+31 of sequence b:
-// W_init[b] (fp32) when given, else W_down0 (bf16).
+// W_init[b] (fp32) when given, else W_down0 (bf16), else zero (a plain reduction over tokens).
 __device__ __forceinline__ void load_init32(const Params& p, int b, int row, int col, uint32_t (&r)[32]) {
   const bool row_ok = row < p.d;
+  if (p.W_init == nullptr && p.W0 == nullptr) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) r[e] = 0u;
+    return;
+  }
   if (p.W_init != nullptr) {
     const float* src = p.W_init + ((int64_t)b * p.d + row) * p.f;
 #pragma unroll
@@ -175,7 +189,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&map_z);
     bool ok = true;
     for (int pr = blockIdx.x; pr < pairs && ok; pr += gridDim.x) {
-      for (int i = 0; i < p.n_chunks && ok; ++i) {
+      for (int j = 0; j < p.n_chunks && ok; ++j) {
+        const int i = chunk_at(p, j);
         const int nkb = chunk_kblocks(p, i);
         for (int slot = 0; slot < 2 && ok; ++slot) {
           const int u = 2 * pr + slot;
@@ -212,8 +227,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t snap_waits[2] = {0, 0};
     bool ok = true;
     for (int pr = blockIdx.x; pr < pairs && ok; pr += gridDim.x) {
-      for (int i = 0; i < p.n_chunks && ok; ++i) {
-        const int nkb = chunk_kblocks(p, i);
+      for (int j = 0; j < p.n_chunks && ok; ++j) {
+        const int nkb = chunk_kblocks(p, chunk_at(p, j));
         for (int slot = 0; slot < 2 && ok; ++slot) {
           const int u = 2 * pr + slot;
           if (u >= p.units) break;
@@ -274,7 +289,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_st32(t_row + c * 32, r);
         }
         tmem_st_wait();
-        if (!p.skip_first) snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks);
+        if (!p.skip_first)
+          snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks + chunk_at(p, 0));
         tc_fence_before();
         mbar_arrive(&snap_done[slot]);
       }
@@ -293,7 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           decode_unit(p, u, b, mb, nb);
           const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BNF);
           if (i < p.n_chunks) {
-            snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks + i);
+            snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks + chunk_at(p, i));
             tc_fence_before();
             mbar_arrive(&snap_done[slot]);
           } else {

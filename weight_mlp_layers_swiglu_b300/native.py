@@ -47,6 +47,10 @@ _SIGNATURES = {
     "ipttt_layer_forward_host": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float,
                                                                           ctypes.c_int, c_vp, c_vp, c_vp,
                                                                           ctypes.c_size_t]),
+    "ipttt_backward_workspace_size": (ctypes.c_int,
+                                      [c_i64] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "ipttt_layer_backward": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int]
+                             + [c_vp] * 10 + [ctypes.c_size_t]),
     "ipttt_swiglu": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, c_vp]),
     "ipttt_target": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_int, c_vp, c_vp]),
     "ipttt_chunk_state": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 5 + [ctypes.c_int, c_vp, c_vp]),
@@ -105,6 +109,14 @@ def workspace_size(B, T, d, d_ff, C, k, dtype: int, host: bool = False) -> int:
     st = fn(B, T, d, d_ff, C, k, dtype, ctypes.byref(out))
     if st != IPTTT_OK:
         raise IptttError(st, f"workspace_size(B={B}, T={T}, d={d}, d_ff={d_ff}, C={C}, k={k})")
+    return out.value
+
+
+def backward_workspace_size(B, T, d, d_ff, C, k, dtype: int) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().ipttt_backward_workspace_size(B, T, d, d_ff, C, k, dtype, ctypes.byref(out))
+    if st != IPTTT_OK:
+        raise IptttError(st, f"backward_workspace_size(B={B}, T={T}, d={d}, d_ff={d_ff}, C={C}, k={k})")
     return out.value
 
 
@@ -218,6 +230,41 @@ class Context:
                                           _ptr(O), _ptr(W_final), _ptr(ws), ws.numel() * ws.element_size())
         self._check(st, "layer_forward")
         return O, W_final
+
+    def layer_backward(self, H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, dO,
+                       dW_final=None, workspace=None):
+        """Gradients of the layer for upstream gradients dO [B,T,d] (and dW_final [B,d,d_ff] fp32,
+        None = zero).  Returns a dict: H, X0 (the activations' dtype) and W_gate, W_up, W_down0,
+        W_target (None without a projection), conv_w (fp32, summed over the batch)."""
+        B, T, d = H.shape
+        f = W_gate.shape[0]
+        k = conv_w.shape[1]
+        dt, dev = H.dtype, self.device
+        for t, n, s in ((H, "H", (B, T, d)), (X0, "X0", (B, T, d)), (W_gate, "W_gate", (f, d)),
+                        (W_up, "W_up", (f, d)), (W_down0, "W_down0", (d, f)), (conv_w, "conv_w", (d, k)),
+                        (dO, "dO", (B, T, d))):
+            _need(t, n, s, dt, dev)
+        if W_target is not None:
+            _need(W_target, "W_target", (d, d), dt, dev)
+        if dW_final is not None:
+            _need(dW_final, "dW_final", (B, d, f), torch.float32, dev)
+        code = dtype_code(dt)
+        f32 = dict(dtype=torch.float32, device=dev)
+        g = {"H": torch.empty((B, T, d), dtype=dt, device=dev), "X0": torch.empty((B, T, d), dtype=dt, device=dev),
+             "W_gate": torch.empty((f, d), **f32), "W_up": torch.empty((f, d), **f32),
+             "W_down0": torch.empty((d, f), **f32),
+             "W_target": torch.empty((d, d), **f32) if W_target is not None else None,
+             "conv_w": torch.empty((d, k), **f32)}
+        if workspace is None:
+            n = backward_workspace_size(B, T, d, f, C, k, code)
+            workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+        st = self.lib.ipttt_layer_backward(
+            self.h, _ptr(H), _ptr(X0), _ptr(W_gate), _ptr(W_up), _ptr(W_down0), _ptr(W_target), _ptr(conv_w),
+            B, T, d, f, C, k, float(eta), code, _ptr(dO), _ptr(dW_final), _ptr(g["H"]), _ptr(g["X0"]),
+            _ptr(g["W_gate"]), _ptr(g["W_up"]), _ptr(g["W_down0"]), _ptr(g["W_target"]), _ptr(g["conv_w"]),
+            _ptr(workspace), workspace.numel() * workspace.element_size())
+        self._check(st, "layer_backward")
+        return g
 
     def layer_resume(self, H, X0, W_gate, W_up, W_target, conv_w, W_state, X0_halo, C: int, eta: float,
                      O=None, W_state_out=None, X0_halo_out=None, workspace=None):
