@@ -398,6 +398,76 @@ def run_cp(args, w):
     return 0
 
 
+def backward_flops(w) -> dict:
+    """Tensor-core FLOPs of one backward call: the gradients proper (algorithmic) and what the
+    call executes, which adds the recomputed forward pieces (Z with [A|U], V, the chunk weights)."""
+    BT, d, f = w.B * w.T, w.d, w.d_ff
+    grads = (2 + 4 + 4 + 4 + 2) * BT * d * f + (2 + 2) * BT * d * d  # R scan, dZ, dH, dW_gate+dW_up, dV; dY, dW_target
+    recompute = (4 + 2) * BT * d * f + 2 * BT * d * d               # Z and [A|U], the W_i scan; V
+    return {"algorithmic": float(grads), "executed": float(grads + recompute)}
+
+
+def run_backward_bench(args, w):
+    """Throughput of the layer's backward pass (ipttt_layer_backward) on one GPU: one step = the
+    gradients of every input and weight for one batch of the workload, given dO and dW_final."""
+    import torch
+
+    import weight_mlp_layers_swiglu_b300 as pkg
+    from weight_mlp_layers_swiglu_b300.inputs import make_activations, make_weights
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    weights = {k: v.to(dev) for k, v in make_weights(w).items()}
+    acts = [make_activations(w, b) for b in range(w.B)]
+    H = torch.stack([a[0] for a in acts]).to(dev)
+    X0 = torch.stack([a[1] for a in acts]).to(dev)
+    g = torch.Generator(device="cpu").manual_seed(1234)
+    dO = torch.randn((w.B, w.T, w.d), generator=g).to(H.dtype).to(dev)
+    dWf = (torch.randn((w.B, w.d, w.d_ff), generator=g) * 0.01).to(dev)
+    ctx = pkg.Context(0)
+    ws = torch.empty(pkg.backward_workspace_size(w.B, w.T, w.d, w.d_ff, w.C, w.k, pkg.dtype_code(H.dtype)),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return ctx.layer_backward(H, X0, weights["W_gate"], weights["W_up"], weights["W_down0"], weights["W_target"],
+                                  weights["conv_w"], w.C, w.eta, dO, dWf, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    if ctx.sync() != 0:
+        raise RuntimeError(f"device status during warm-up: {ctx.last_error()}")
+    with ClockSampler(0) as clocks:
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if ctx.sync() != 0:
+        raise RuntimeError(f"device status in the timed region: {ctx.last_error()}")
+    ms = e0.elapsed_time(e1)
+    peaks, peak_src = load_peaks()
+    fl = backward_flops(w)
+    per_step = ms / args.steps
+    ex = fl["executed"] / (per_step * 1e-3) / 1e12
+    al = fl["algorithmic"] / (per_step * 1e-3) / 1e12
+    line = {"metric": "backward tokens/s per In-Place-TTT MLP layer", "value": w.B * w.T / (per_step * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": workload_config(w) | {"pass": "backward (dO and dW_final given)"},
+            "tflops_executed": ex, "tflops_algorithmic": al,
+            "roofline": {"bound": "tensor", "achieved": ex, "peak": peaks["bf16_tflops_sustained"],
+                         "unit": "TFLOP/s", "frac": ex / peaks["bf16_tflops_sustained"], "traffic": None,
+                         "peak_source": f"{peak_src} bf16 sustained", "flop_per_step": fl},
+            "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+    ctx.close()
+    return 0
+
+
 def e2e_leg(args, w, ctx, weights, H_host, X_host, dev, world):
     """The same metric end to end through the C ABI with host buffers: every step uploads H and
     X0 from pinned memory, runs the layer and downloads O and W_final."""
@@ -538,6 +608,8 @@ def main(argv=None):
     ap.add_argument("--sweep", choices=["chunk", "state"], default=None,
                     help="one line per chunk size C in {256, 512, 1024, 2048} (eta = 1/C) or per state size "
                          "d_ff in {0.5, 1, 4} x the workload's (the axes of the pages' ablations)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the layer's backward pass instead (one GPU; its own JSON line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -550,6 +622,8 @@ def main(argv=None):
         return run_reference(args, w)
     if args.cp:
         return run_cp(args, w)
+    if args.backward:
+        return run_backward_bench(args, w)
     if args.sweep:
         args.no_e2e, args.no_cpu_baseline, args.stream_tokens = True, True, 0
         if args.sweep == "chunk":

@@ -55,6 +55,7 @@ def _check(g, ref, tol):
         assert g[n].shape == ref[n].shape, n
         assert torch.isfinite(g[n].float()).all(), n
         errs[n] = rel_err(g[n], ref[n])
+    print({n: f"{e:.2e}" for n, e in errs.items()})
     bad = {n: e for n, e in errs.items() if not e <= tol}
     assert not bad, f"gradients past {tol}: {bad} (all: {errs})"
     return errs
@@ -138,3 +139,37 @@ def test_backward_rejects_small_workspace_and_overlap(ctx):
         ctx.layer_backward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
                            xd["conv_w"], 128, 0.1, dO_alias, workspace=big)
     assert e.value.status == 1
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,T", [("small_0p4b", None), ("qwen3_4b_32k", 4096), ("serve_8x8k", 1024)])
+def test_backward_at_workload_widths(ctx, name, T):
+    """The bf16 workloads' own shapes (the 0.4B-scale layer at its full 32k tokens; the 4B-shaped
+    layers at their full widths over a shorter prefix, which the float64 autograd oracle finishes
+    in seconds) against the oracle, every gradient element by element."""
+    import json
+    import os
+
+    from weight_mlp_layers_swiglu_b300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[name]
+    if T is not None:
+        w = w.with_(T=T)
+    x = make_inputs(w)
+    dO = seeded((w.B, w.T, w.d), 1.0, torch.bfloat16, 77)
+    dWf = seeded((w.B, w.d, w.d_ff), 0.05, torch.float32, 78)
+    xd = to_dev(x)
+    g = ctx.layer_backward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
+                           xd["conv_w"], w.C, w.eta, dO.cuda(), dWf.cuda())
+    assert ctx.sync() == 0, ctx.last_error()
+    g = {n: (None if v is None else v.cpu()) for n, v in g.items()}
+    del xd
+    torch.cuda.empty_cache()
+    ref = layer_backward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"], x["conv_w"], w.C,
+                         w.eta, dO, dWf)
+    errs = _check(g, ref, TOL["bf16"])
+    out = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
+    if os.path.isdir(out):
+        with open(os.path.join(out, f"parity_backward_{name}_T{w.T}.json"), "w") as f:
+            json.dump({"workload": name, "T": w.T, **errs}, f)
+    print(name, w.T, errs)
