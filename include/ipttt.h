@@ -198,9 +198,9 @@ ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const 
  * The forward quantities (Z, A, U, Y, V and every W_i) are recomputed, not passed in. */
 
 /* Bytes of device workspace ipttt_layer_backward needs (host-only call).  Layout: Y, V [B,T,d],
- * Z [B,T,d_ff], [A|U] [B,T,2*d_ff], dZ [B,T,d_ff], dV, dY [B,T,d], the W_i and R_i stacks
- * [B,ceil(T/C),d,d_ff] (all dtype), per-sequence dW_down0 [B,d,d_ff] fp32 and the conv-tap
- * partial sums [B*ceil(T/256),d,k] fp32; each region 256-byte aligned.  Errors as
+ * Z [B,T,d_ff], [A|U] [B,T,2*d_ff], dZ [B,T,d_ff] (fp32 only), dV, dY [B,T,d], the W_i and
+ * R_i stacks [B,ceil(T/C),d,d_ff] (all dtype), per-sequence dW_down0 [B,d,d_ff] fp32 and the
+ * conv-tap partial sums [B*ceil(T/64),d,k] fp32; each region 256-byte aligned.  Errors as
  * ipttt_workspace_size. */
 ipttt_status ipttt_backward_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
                                            ipttt_dtype dtype, size_t* bytes);
@@ -216,8 +216,10 @@ ipttt_status ipttt_backward_workspace_size(int64_t B, int64_t T, int64_t d, int6
  *   dconv_w   [d, k]           fp32,  device
  *   workspace                  device, >= ipttt_backward_workspace_size() bytes, overwritten
  * bf16: every product on the tensor cores with fp32 accumulation; the intermediates (Z, V,
- * W_i, R_i, dZ, dA, dU, dV, dY) are rounded to bf16 between steps.  B*T = 0 writes zeros
- * (dW_down0 = sum_b dW_final[b]).  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+ * W_i, R_i, dA, dU, dV, dY) are rounded to bf16 between steps (dZ stays fp32: the SwiGLU
+ * adjoints are taken in the epilogue of the GEMM that forms it).  B*T = 0 writes zeros
+ * (dW_down0 = sum_b dW_final[b]).  Also requires B <= 65535 and T <= 524280.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
                                   const void* W_up, const void* W_down0, const void* W_target,
                                   const void* conv_w, int64_t B, int64_t T, int64_t d, int64_t d_ff,

@@ -597,9 +597,12 @@ ipttt_status launch_state_general(ipttt_ctx* ctx, const void* V, int64_t v_strid
 
 // C = A1 B1 + A2 B2 (bf16, kTwoSeg): A segments token-major [B, T, K] (a2 = A1's map shifted by
 // a2_koff columns when a2 is NULL), B segments [slices, K, N]; per chunk when b_per_problem.
+// With au != NULL, C is dZ and is not stored: the epilogue turns au = [A | U] ([B*T, 2N]) into
+// [dA | dU] in place (out is then unused and may be NULL).
 ipttt_status launch_two_seg(ipttt_ctx* ctx, const void* A1, int64_t a1_stride, const void* A2, int64_t a2_stride,
                             int64_t a2_koff, const void* B1, const void* B2, int64_t b_slices, bool b_per_problem,
-                            int64_t B, int64_t T, int64_t C, int64_t K1, int64_t K2, int64_t N, void* out) {
+                            int64_t B, int64_t T, int64_t C, int64_t K1, int64_t K2, int64_t N, void* out,
+                            void* au = nullptr) {
   const int64_t n = n_chunks_of(T, C);
   CUtensorMap ma1, ma2, mb1, mb2, mo;
   // segment 1 is cut at K1 columns (its ragged K block reads zeros, not segment 2); without its
@@ -608,9 +611,13 @@ ipttt_status launch_two_seg(ipttt_ctx* ctx, const void* A1, int64_t a1_stride, c
   if (!map_3d_strided(ctx, &ma1, A1, B, T, K1, a1_stride, 128) ||
       !map_3d_strided(ctx, &ma2, shared ? A1 : A2, B, T, shared ? a2_koff + K2 : K2, shared ? a1_stride : a2_stride,
                       128) ||
-      !map_3d(ctx, &mb1, B1, b_slices, K1, N, 64) || !map_3d(ctx, &mb2, B2, b_slices, K2, N, 64) ||
-      !map_3d(ctx, &mo, out, B, T, N, 32))
+      !map_3d(ctx, &mb1, B1, b_slices, K1, N, 64) || !map_3d(ctx, &mb2, B2, b_slices, K2, N, 64))
     return IPTTT_ERR_CUDA;
+  if (out != nullptr) {
+    if (!map_3d(ctx, &mo, out, B, T, N, 32)) return IPTTT_ERR_CUDA;
+  } else {
+    mo = ma1;  // never stored through
+  }
   gemm::Params p{};
   p.m_tiles = (int)(C / gemm::BM);
   p.n_tiles = ceil_div(N, gemm::BN);
@@ -618,6 +625,8 @@ ipttt_status launch_two_seg(ipttt_ctx* ctx, const void* A1, int64_t a1_stride, c
   p.k_blocks2 = ceil_div(K2, gemm::BK);
   p.a2_koff = shared ? (int)a2_koff : 0;
   p.b_per_problem = b_per_problem ? 1 : 0;
+  p.au = static_cast<__nv_bfloat16*>(au);
+  p.au_f = (int)N;
   p.problems = (int)(B * n);
   p.group_m = 16;
   p.scale = 1.f;
@@ -668,7 +677,7 @@ BwdLayout bwd_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, int 
   L.v = take((size_t)B * T * d * es);
   L.z = take((size_t)B * T * f * es);
   L.au = take((size_t)B * T * 2 * f * es);
-  L.dz = take((size_t)B * T * f * es);
+  L.dz = take(dt == IPTTT_BF16 ? 0 : (size_t)B * T * f * es);  // bf16: dZ never leaves the GEMM epilogue
   L.dv = take((size_t)B * T * d * es);
   L.dy = take((size_t)B * T * d * es);
   L.wst = take((size_t)B * n * d * f * es);
@@ -753,11 +762,13 @@ ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const v
   if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, dW0b, false)) != IPTTT_OK) return s;
   if (bf16) {
     // reverse scan: R_i = dW_final + sum_{l>i} dO_l^T Z_l, final = dW_final + sum_i dO_i^T Z_i
-    if ((s = launch_state_general(ctx, dO, d, Z, f, B, T, d, f, C, nullptr, dW_final, false, true, Rst, dW0b)) !=
-        IPTTT_OK)
+    if ((s = launch_state_general(ctx, dO, d, Z, f, B, T, d, f, C, nullptr, dW_final, false, true, Rst,
+                                  B == 1 ? dW0 : dW0b)) != IPTTT_OK)
       return s;
-    // dZ_i = dO_i W_i + V_i R_i (V carries eta)
-    if ((s = launch_two_seg(ctx, dO, d, V, d, 0, Wst, Rst, B * n, true, B, T, C, d, d, f, dZ)) != IPTTT_OK) return s;
+    // dZ_i = dO_i W_i + V_i R_i (V carries eta), and in the same epilogue the gated-MLP
+    // adjoints: AU = [A | U] becomes [dA | dU]
+    if ((s = launch_two_seg(ctx, dO, d, V, d, 0, Wst, Rst, B * n, true, B, T, C, d, d, f, nullptr, AU)) != IPTTT_OK)
+      return s;
   } else {
     float* rst = static_cast<float*>(Rst);
     // G_i = dO_i^T Z_i per chunk, then the reverse exclusive scan
@@ -765,7 +776,8 @@ ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const v
                    0.f, 2, T, C, n, B, d, f, 0, 0, 0, df)) != IPTTT_OK)
       return s;
     dim3 g2(ceil_div(df, 256), (unsigned)B);
-    simt::chunk_scan_f32_kernel<<<g2, 256, 0, ctx->stream>>>(rst, nullptr, dW0b, (int)B, (int)n, df, dW_final, 1);
+    simt::chunk_scan_f32_kernel<<<g2, 256, 0, ctx->stream>>>(rst, nullptr, B == 1 ? dW0 : dW0b, (int)B, (int)n, df,
+                                                             dW_final, 1);
     if ((s = check_launch(ctx, "reverse scan launch")) != IPTTT_OK) return s;
     // dZ_i = dO_i W_i + V_i R_i
     if ((s = sgemm(ctx, static_cast<const float*>(dO), d, 1, static_cast<const float*>(Wst), f, 1,
@@ -774,14 +786,12 @@ ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const v
                    1, T, C, n, B, d, 0, f, 0, df, 0)) != IPTTT_OK)
       return s;
   }
-  // gated-MLP backward in place: AU -> [dA | dU]
-  if (bf16)
-    simt::swiglu_backward_kernel<__nv_bfloat16><<<ceil_div(BT * f, 256), 256, 0, ctx->stream>>>(
-        static_cast<const __nv_bfloat16*>(dZ), static_cast<__nv_bfloat16*>(AU), BT, (int)f);
-  else
+  // fp32: the gated-MLP backward in place, AU -> [dA | dU] (bf16 did it in the dZ epilogue)
+  if (!bf16) {
     simt::swiglu_backward_kernel<float><<<ceil_div(BT * f, 256), 256, 0, ctx->stream>>>(
         static_cast<const float*>(dZ), static_cast<float*>(AU), BT, (int)f);
-  if ((s = check_launch(ctx, "swiglu backward launch")) != IPTTT_OK) return s;
+    if ((s = check_launch(ctx, "swiglu backward launch")) != IPTTT_OK) return s;
+  }
   if (bf16) {
     const size_t es = 2;
     // dH = dA W_gate + dU W_up
@@ -822,28 +832,29 @@ ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const v
   }
   // the causal conv's adjoints
   {
-    const int64_t nx = BT * d;
-    dim3 gw(ceil_div(d, 128), (unsigned)L.strips);
+    const int64_t groups = d / (bf16 ? 8 : 4);  // 16-byte channel groups
+    dim3 gx(ceil_div(groups, 64), ceil_div(T, simt::CONVX_ROWS), (unsigned)B);
+    dim3 gw((unsigned)L.strips, ceil_div(groups, 64));
     if (bf16) {
-      simt::conv_backward_x_kernel<__nv_bfloat16><<<ceil_div(nx, 256), 256, 0, ctx->stream>>>(
+      simt::conv_backward_x_kernel<__nv_bfloat16><<<gx, 64, 0, ctx->stream>>>(
           static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(cw), static_cast<__nv_bfloat16*>(dX0),
           (int)B, (int)T, (int)d, k, ctx->target_shift);
-      simt::conv_backward_w_partial_kernel<__nv_bfloat16><<<gw, 128, 0, ctx->stream>>>(
+      simt::conv_backward_w_partial_kernel<__nv_bfloat16><<<gw, 64, 0, ctx->stream>>>(
           static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(X0), part, (int)B, (int)T, (int)d, k,
           ctx->target_shift);
     } else {
-      simt::conv_backward_x_kernel<float><<<ceil_div(nx, 256), 256, 0, ctx->stream>>>(
+      simt::conv_backward_x_kernel<float><<<gx, 64, 0, ctx->stream>>>(
           static_cast<const float*>(dY), static_cast<const float*>(cw), static_cast<float*>(dX0), (int)B, (int)T,
           (int)d, k, ctx->target_shift);
-      simt::conv_backward_w_partial_kernel<float><<<gw, 128, 0, ctx->stream>>>(
+      simt::conv_backward_w_partial_kernel<float><<<gw, 64, 0, ctx->stream>>>(
           static_cast<const float*>(dY), static_cast<const float*>(X0), part, (int)B, (int)T, (int)d, k,
           ctx->target_shift);
     }
     simt::sum_strips_kernel<<<ceil_div(d * k, 256), 256, 0, ctx->stream>>>(part, dcw, (int)L.strips, d * k);
     if ((s = check_launch(ctx, "conv backward launch")) != IPTTT_OK) return s;
   }
-  // the shared initial fast weight: sum over sequences
-  simt::sum_strips_kernel<<<ceil_div(df, 256), 256, 0, ctx->stream>>>(dW0b, dW0, (int)B, df);
+  // the shared initial fast weight: sum over sequences (one sequence wrote it directly)
+  if (B > 1) simt::sum_strips_kernel<<<ceil_div(df, 256), 256, 0, ctx->stream>>>(dW0b, dW0, (int)B, df);
   return check_launch(ctx, "batch sum launch");
 }
 
@@ -1221,8 +1232,8 @@ ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0,
     set_err(ctx, "B*T must be < 2^31");
     return IPTTT_ERR_UNSUPPORTED;
   }
-  if (B > 65535 || B * ((T + simt::CONVW_STRIP - 1) / simt::CONVW_STRIP) > 65535) {
-    set_err(ctx, "B (%lld) and B*ceil(T/%d) must be <= 65535", (long long)B, simt::CONVW_STRIP);
+  if (B > 65535 || (T + simt::CONVX_ROWS - 1) / simt::CONVX_ROWS > 65535) {
+    set_err(ctx, "B (%lld) and ceil(T/%d) must be <= 65535", (long long)B, simt::CONVX_ROWS);
     return IPTTT_ERR_UNSUPPORTED;
   }
   const bool work = B > 0 && T > 0;

@@ -292,50 +292,91 @@ __global__ void swiglu_backward_kernel(const T* __restrict__ dZ, T* __restrict__
 }
 
 // Adjoint of the causal depthwise conv for its input: with the window shifted by `shift` tokens,
-// dX0[u, c] = sum_s w[c, s] dY[u - shift + (k-1) - s, c] over the rows that exist.
+// dX0[u, c] = sum_s w[c, s] dY[u - shift + (k-1) - s, c] over the rows that exist.  Grid:
+// x = blocks of 16-byte channel groups, y = blocks of CONVX_ROWS tokens, z = sequence; each
+// thread keeps its channels' taps in registers and produces CONVX_ROWS rows.
+constexpr int CONVX_ROWS = 8;
+
 template <typename T>
 __global__ void conv_backward_x_kernel(const T* __restrict__ dY, const T* __restrict__ conv_w, T* __restrict__ dX0,
                                        int B, int T_len, int d, int k, int shift) {
-  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t n = (int64_t)B * T_len * d;
-  if (e >= n) return;
-  const int c = (int)(e % d);
-  const int64_t bt = e / d;
-  const int t = (int)(bt % T_len);
-  const int64_t base = bt - t;  // b * T_len
-  float acc = 0.f;
-  for (int s = 0; s < k; ++s) {
-    const int src = t - shift + (k - 1) - s;
-    if (src >= 0 && src < T_len) acc = fmaf(static_cast<float>(conv_w[(int64_t)c * k + s]), ld_f(dY + (base + src) * d + c), acc);
+  constexpr int VEC = 16 / sizeof(T);
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= d / VEC) return;
+  const int c0 = g * VEC;
+  const int t0 = blockIdx.y * CONVX_ROWS;
+  const int64_t base = (int64_t)blockIdx.z * T_len;
+  float w[8][VEC];  // k <= 8
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) w[s][j] = s < k ? static_cast<float>(conv_w[(int64_t)(c0 + j) * k + s]) : 0.f;
+  for (int t = t0; t < min(t0 + CONVX_ROWS, T_len); ++t) {
+    float acc[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int src = t - shift + (k - 1) - s;
+      if (s >= k || src < 0 || src >= T_len) continue;
+      const uint4 raw = *reinterpret_cast<const uint4*>(dY + (base + src) * d + c0);
+      const T* v = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) acc[j] = fmaf(w[s][j], static_cast<float>(v[j]), acc[j]);
+    }
+    uint4 out;
+    T* o = reinterpret_cast<T*>(&out);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) o[j] = static_cast<T>(acc[j]);
+    *reinterpret_cast<uint4*>(dX0 + (base + t) * d + c0) = out;
   }
-  st_f(dX0 + e, acc);
 }
 
 // Adjoint for the taps, in two passes (deterministic): partial[strip, c, s] = sum over the strip's
 // tokens of dY[t, c] X0[t + shift - (k-1) + s, c]; then dconv_w[c, s] = sum over strips in order.
-constexpr int CONVW_STRIP = 256;
+// Grid: x = strip (B * ceil(T / CONVW_STRIP)), y = blocks of 16-byte channel groups.
+constexpr int CONVW_STRIP = 64;
 
 template <typename T>
 __global__ void conv_backward_w_partial_kernel(const T* __restrict__ dY, const T* __restrict__ X0,
                                                float* __restrict__ partial, int B, int T_len, int d, int k,
                                                int shift) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  const int strip = blockIdx.y;  // over B * ceil(T / CONVW_STRIP)
+  constexpr int VEC = 16 / sizeof(T);
+  const int g = blockIdx.y * blockDim.x + threadIdx.x;
+  if (g >= d / VEC) return;
+  const int c0 = g * VEC;
+  const int strip = blockIdx.x;
   const int per_b = (T_len + CONVW_STRIP - 1) / CONVW_STRIP;
-  if (c >= d) return;
   const int b = strip / per_b;
   const int t0 = (strip % per_b) * CONVW_STRIP;
   const int t1 = min(t0 + CONVW_STRIP, T_len);
-  const T* dy = dY + (int64_t)b * T_len * d + c;
-  const T* x = X0 + (int64_t)b * T_len * d + c;
-  for (int s = 0; s < k; ++s) {
-    float acc = 0.f;
-    for (int t = t0; t < t1; ++t) {
+  const T* dy = dY + (int64_t)b * T_len * d + c0;
+  const T* x = X0 + (int64_t)b * T_len * d + c0;
+  float acc[8][VEC];  // k <= 8
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[s][j] = 0.f;
+#pragma unroll 4
+  for (int t = t0; t < t1; ++t) {
+    const uint4 rd = *reinterpret_cast<const uint4*>(dy + (int64_t)t * d);
+    const T* dv = reinterpret_cast<const T*>(&rd);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
       const int src = t + shift - (k - 1) + s;
-      if (src >= 0 && src < T_len) acc = fmaf(ld_f(dy + (int64_t)t * d), ld_f(x + (int64_t)src * d), acc);
+      if (s >= k || src < 0 || src >= T_len) continue;
+      const uint4 rx = *reinterpret_cast<const uint4*>(x + (int64_t)src * d);
+      const T* xv = reinterpret_cast<const T*>(&rx);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) acc[s][j] = fmaf(static_cast<float>(dv[j]), static_cast<float>(xv[j]), acc[s][j]);
     }
-    partial[((int64_t)strip * d + c) * k + s] = acc;
   }
+  float* out = partial + ((int64_t)strip * d + c0) * k;
+#pragma unroll
+  for (int j = 0; j < VEC; ++j)
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < k) out[j * k + s] = acc[s][j];
 }
 
 __global__ void sum_strips_kernel(const float* __restrict__ partial, float* __restrict__ out, int strips, int64_t n) {

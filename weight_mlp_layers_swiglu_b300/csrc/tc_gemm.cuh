@@ -58,6 +58,11 @@ struct Params {
   int k_blocks2;       // kTwoSeg: k-blocks of the second segment (the first has k_blocks)
   int a2_koff;         // kTwoSeg: column offset of the second segment within its A map
   int b_per_problem;   // kTwoSeg: 1 = each problem (chunk) has its own B slice, 0 = one shared B
+  // kTwoSeg, optional: the result is dZ and is not stored; instead the SwiGLU adjoints overwrite
+  // the saved pre-activations au = [A | U] ([B*T, 2*au_f] bf16, the output's rows):
+  // dA = dZ U s (1 + A (1 - s)), dU = dZ A s with s = sigmoid(A)
+  __nv_bfloat16* au;
+  int au_f;
   DevStatus st;
 };
 
@@ -280,6 +285,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   pre[c * 16 + e] = pack_bf16x2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1]));
               }
               out.put(pre, &map_x, nt * 128 + h * 64, part, mt * BM + q * 32);
+            }
+          }
+        }
+      } else if (KIND == kTwoSeg && p.au != nullptr) {
+        const int bq = prob / p.n_chunks;
+        const int i = prob - bq * p.n_chunks;
+        const int tok = i * p.C + mt * BM + q * 32 + lane;
+        __nv_bfloat16* au_row = p.au + ((int64_t)bq * p.T + tok) * (2 * (int64_t)p.au_f);
+#pragma unroll 1
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t lo[32], hi[32];
+          tmem_ld32(t_row + h * 64, lo);
+          tmem_ld32(t_row + h * 64 + 32, hi);
+          tmem_ld_wait(lo);
+          tmem_ld_wait(hi);
+          const int n0 = nt * BN + h * 64;
+          if (tok < p.T) {
+            // 8 groups of 8 columns; d_ff % 8 == 0, so a group lies wholly inside or outside
+            uint4 av[8], uv[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              if (n0 + v * 8 < p.au_f) {
+                av[v] = *reinterpret_cast<const uint4*>(au_row + n0 + v * 8);
+                uv[v] = *reinterpret_cast<const uint4*>(au_row + p.au_f + n0 + v * 8);
+              }
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              if (n0 + v * 8 >= p.au_f) continue;
+              const uint32_t* aw = reinterpret_cast<const uint32_t*>(&av[v]);
+              const uint32_t* uw = reinterpret_cast<const uint32_t*>(&uv[v]);
+              uint4 da, du;
+              uint32_t* daw = reinterpret_cast<uint32_t*>(&da);
+              uint32_t* duw = reinterpret_cast<uint32_t*>(&du);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float ga[2], gd[2];
+                const float A0 = bf16_lo(aw[e]), A1 = bf16_hi(aw[e]);
+                const float U0 = bf16_lo(uw[e]), U1 = bf16_hi(uw[e]);
+                const int j = (v & 3) * 8 + 2 * e;
+                const float z0 = __uint_as_float(v < 4 ? lo[j] : hi[j]);
+                const float z1 = __uint_as_float(v < 4 ? lo[j + 1] : hi[j + 1]);
+                const float s0 = 1.0f / (1.0f + __expf(-A0)), s1 = 1.0f / (1.0f + __expf(-A1));
+                ga[0] = z0 * U0 * s0 * (1.0f + A0 * (1.0f - s0));
+                ga[1] = z1 * U1 * s1 * (1.0f + A1 * (1.0f - s1));
+                gd[0] = z0 * A0 * s0;
+                gd[1] = z1 * A1 * s1;
+                daw[e] = pack_bf16x2(ga[0], ga[1]);
+                duw[e] = pack_bf16x2(gd[0], gd[1]);
+              }
+              *reinterpret_cast<uint4*>(au_row + n0 + v * 8) = da;
+              *reinterpret_cast<uint4*>(au_row + p.au_f + n0 + v * 8) = du;
             }
           }
         }
