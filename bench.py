@@ -267,6 +267,7 @@ def run_ours(args, w):
     H = H_host.to(dev)
     X0 = X_host.to(dev)
     ctx = pkg.Context(local)
+    ctx.set_cta_pairs(not args.single_cta)
     stream = torch.cuda.current_stream(dev)
     O = torch.empty((w.B, w.T, w.d), dtype=H.dtype, device=dev)
     Wf = torch.empty((w.B, w.d, w.d_ff), dtype=torch.float32, device=dev)
@@ -544,7 +545,8 @@ def finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks,
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": workload_config(w) | {"parallelism": f"replicas x{world} (one sequence set per GPU)"},
+            "config": workload_config(w) | {"parallelism": f"replicas x{world} (one sequence set per GPU)",
+                                            "gemm_tiles": "single CTA" if args.single_cta else "CTA pairs"},
             "tflops": layer_tflops, "frac_bf16_peak": layer_tflops / peaks["bf16_tflops"] / world,
             "frac_bf16_peak_sustained": layer_tflops / peaks["bf16_tflops_sustained"] / world,
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches * world if timed_calls == args.steps
@@ -608,6 +610,8 @@ def main(argv=None):
     ap.add_argument("--sweep", choices=["chunk", "state"], default=None,
                     help="one line per chunk size C in {256, 512, 1024, 2048} (eta = 1/C) or per state size "
                          "d_ff in {0.5, 1, 4} x the workload's (the axes of the pages' ablations)")
+    ap.add_argument("--single-cta", action="store_true",
+                    help="run the bf16 GEMMs on single CTAs instead of CTA pairs (for comparison)")
     ap.add_argument("--backward", action="store_true",
                     help="time the layer's backward pass instead (one GPU; its own JSON line)")
     args = ap.parse_args(argv)

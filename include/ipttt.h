@@ -94,6 +94,12 @@ ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* cuda_stream);
  * cooperative launch always use two. */
 ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable);
 
+/* Choose how the bf16 GEMMs of steps (1), (2) and (5) run: enable = 1 (default) on CTA pairs
+ * (clusters of two SMs issuing tcgen05.mma.cta_group::2 on 256-row tiles; the chunk apply
+ * only when C % 256 == 0), 0 on single CTAs (128-row tiles).  Results are bit-identical:
+ * every output element is the same fp32 sum in the same order, only the tiling differs. */
+ipttt_status ipttt_set_cta_pairs(ipttt_ctx* ctx, int enable);
+
 /* Ablation variant of the target (zhichai.net page §6, conv/proj ablation; its Theorem 1 uses
  * the next token's embedding as target): shift = 1 moves the conv window one token later, so
  * that the target of token t ends at X0[t+1] (the token after a call's last one reads as

@@ -1,0 +1,83 @@
+"""The bf16 GEMMs on CTA pairs (tcgen05.mma.cta_group::2, 256-row tiles) against the same GEMMs on
+single CTAs (128-row tiles), through the C ABI: every output element is the same fp32 sum of the
+same products in the same K order, so the two tilings must agree bit for bit.  The shapes end in
+ragged tails (rows that fill only the even CTA of the last pair, ragged d and d_ff) and the
+oracle bounds the pair path too (the step tests run it by default)."""
+import pytest
+import torch
+
+from oracle import oracle
+from tests.util import TOL, rel_err, seeded, to_dev
+from weight_mlp_layers_swiglu_b300.inputs import random_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import weight_mlp_layers_swiglu_b300 as pkg
+
+    c = pkg.Context(0)
+    yield c
+    c.set_cta_pairs(True)
+    c.close()
+
+
+def both(ctx, fn):
+    ctx.set_cta_pairs(True)
+    a = fn()
+    assert ctx.sync() == 0, ctx.last_error()
+    ctx.set_cta_pairs(False)
+    b = fn()
+    assert ctx.sync() == 0, ctx.last_error()
+    ctx.set_cta_pairs(True)
+    return a, b
+
+
+@pytest.mark.parametrize("rows,d,f", [(300, 256, 384), (128, 64, 128), (1, 136, 264), (1000, 512, 1024),
+                                      (257, 2560, 1024)])
+def test_swiglu_pairs_match_single(ctx, rows, d, f):
+    H = seeded((rows, d), 1.0, torch.bfloat16, 1, "cuda")
+    Wg = seeded((f, d), d ** -0.5, torch.bfloat16, 2, "cuda")
+    Wu = seeded((f, d), d ** -0.5, torch.bfloat16, 3, "cuda")
+    a, b = both(ctx, lambda: ctx.swiglu(H, Wg, Wu).clone())
+    assert torch.equal(a, b)
+    assert rel_err(a, oracle.swiglu(H.cpu(), Wg.cpu(), Wu.cpu())) <= 1e-2
+
+
+@pytest.mark.parametrize("B,T,d", [(2, 200, 320), (1, 300, 256), (3, 77, 128), (1, 600, 2560)])
+def test_target_pairs_match_single(ctx, B, T, d):
+    X0 = seeded((B, T, d), 0.02, torch.bfloat16, 4, "cuda")
+    cw = seeded((d, 4), 0.5, torch.bfloat16, 5, "cuda")
+    Wt = seeded((d, d), d ** -0.5, torch.bfloat16, 6, "cuda")
+    a, b = both(ctx, lambda: ctx.target(X0, cw, Wt, 1.0 / 128)[0].clone())
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("B,T,d,f,C", [(2, 600, 320, 384, 256), (1, 1024, 256, 1024, 512), (1, 100, 128, 256, 256),
+                                       (2, 300, 192, 384, 128)])
+def test_apply_pairs_match_single(ctx, B, T, d, f, C):
+    n = (T + C - 1) // C
+    Z = seeded((B, T, f), f ** -0.5, torch.bfloat16, 7, "cuda")
+    W = seeded((B * n, d, f), 1.0, torch.bfloat16, 8, "cuda").view(B, n, d, f)
+    a, b = both(ctx, lambda: ctx.chunk_apply(Z, W, C).clone())
+    assert torch.equal(a, b)
+    for bb in range(B):
+        assert rel_err(a[bb], oracle.chunk_apply(Z[bb].cpu(), W[bb].cpu(), C)) <= 1e-2
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("B,T,d,f,C,k", [(2, 700, 256, 512, 256, 4), (1, 1100, 384, 768, 512, 3)])
+def test_layer_pairs_match_single(ctx, fused, B, T, d, f, C, k):
+    w, x = random_case(B, T, d, f, C, k, 2.0 / C, "bf16", 60 + T)
+    xd = to_dev(x)
+    ctx.set_fused_tail(fused)
+    try:
+        (Oa, Wa), (Ob, Wb) = both(ctx, lambda: tuple(t.clone() for t in ctx.layer_forward(
+            xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"], xd["conv_w"], C, w.eta)))
+    finally:
+        ctx.set_fused_tail(True)
+    assert torch.equal(Oa, Ob) and torch.equal(Wa, Wb)
+    O_ref, W_ref = oracle.layer_forward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"],
+                                        x["conv_w"], C, w.eta)
+    assert rel_err(Oa, O_ref) <= TOL["bf16"] and rel_err(Wa, W_ref) <= TOL["bf16"]

@@ -18,6 +18,7 @@
 #include "simt.cuh"
 #include "tc_fused.cuh"
 #include "tc_gemm.cuh"
+#include "tc_gemm2.cuh"
 #include "tc_state.cuh"
 
 using namespace ipttt;
@@ -54,6 +55,8 @@ struct ipttt_ctx {
   bool attrs_set = false;
   bool coop = false;       // device supports cooperative launches
   bool fused_tail = true;  // run steps (3)-(5) as one cooperative kernel when possible
+  bool cta_pairs = true;   // bf16 GEMMs on CTA pairs (cta_group::2) when the device allows
+  int pair_ctas = 0;       // CTAs of the pair GEMM grid (2 x co-resident clusters; 0 = unavailable)
   int target_shift = 0;    // 1: the conv window of the target ends at the next token
   // The causal conv runs on an internal side stream, forked from and joined back into
   // `stream` with these events, so that it overlaps the SwiGLU GEMM.
@@ -267,6 +270,27 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
   e = cudaFuncSetAttribute(gemm::tc_gemm_kernel<gemm::kTwoSeg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            gemm::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (two-segment)");
+  {
+    const void* pk[3] = {(const void*)gemm2::tc_gemm2_kernel<gemm::kSwiglu>,
+                         (const void*)gemm2::tc_gemm2_kernel<gemm::kTarget>,
+                         (const void*)gemm2::tc_gemm2_kernel<gemm::kApply>};
+    int clusters = 1 << 30;
+    for (const void* k : pk) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm2::SMEM_BYTES);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (pair gemm)");
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(ctx->sm_count & ~1), 1, 1);
+      cfg.blockDim = dim3(gemm2::NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = gemm2::SMEM_BYTES;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      clusters = n < clusters ? n : clusters;
+    }
+    ctx->pair_ctas = 2 * clusters;
+  }
   e = cudaFuncSetAttribute(state::tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            state::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (state)");
@@ -278,6 +302,13 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
 }
 
 DevStatus dev_status(ipttt_ctx* ctx) { return DevStatus{ctx->status, ctx->wait_limit_ns}; }
+
+bool use_pairs(const ipttt_ctx* ctx) { return ctx->cta_pairs && ctx->pair_ctas >= 2; }
+
+// Grid of a pair-GEMM launch: one CTA pair per tile, at most the co-resident pairs.
+int pair_grid(const ipttt_ctx* ctx, int64_t tiles) {
+  return 2 * (int)(tiles < ctx->pair_ctas / 2 ? tiles : ctx->pair_ctas / 2);
+}
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
@@ -292,17 +323,23 @@ ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const voi
         !map_2d(ctx, &mb1, Wu, f, d, 64, 128) || !map_2d(ctx, &mo, Z, rows, f, 64, 32))
       return IPTTT_ERR_CUDA;
     gemm::Params p{};
-    p.m_tiles = ceil_div(rows, gemm::BM);
+    const bool pairs = use_pairs(ctx);
+    p.m_tiles = ceil_div(rows, pairs ? gemm2::PAIR_M : gemm::BM);
     p.n_tiles = ceil_div(f, 128);
     p.k_blocks = ceil_div(d, gemm::BK);
     p.problems = 1;
-    p.group_m = 16;
+    p.group_m = pairs ? 8 : 16;
     p.scale = 1.f;
     p.st = dev_status(ctx);
     const int tiles = p.m_tiles * p.n_tiles;
-    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-    gemm::tc_gemm_kernel<gemm::kSwiglu><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb0, mb1, mo,
-                                                                                                    mo, p);
+    if (pairs) {
+      gemm2::tc_gemm2_kernel<gemm::kSwiglu><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
+                                             ctx->stream>>>(ma, mb0, mb1, mo, p);
+    } else {
+      const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+      gemm::tc_gemm_kernel<gemm::kSwiglu><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb0, mb1,
+                                                                                                      mo, mo, p);
+    }
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(H);
@@ -370,10 +407,19 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
     p.zero_ptr = zero_ptr;
     p.zero_count = zero_count;
     p.st = dev_status(ctx);
-    const int tiles = p.m_tiles * p.n_tiles;
-    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-    gemm::tc_gemm_kernel<gemm::kTarget><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, mo, mo,
-                                                                                                    p);
+    const bool pairs = use_pairs(ctx);
+    if (pairs) {
+      p.m_tiles = ceil_div(rows, gemm2::PAIR_M);
+      p.group_m = 8;
+      const int tiles = p.m_tiles * p.n_tiles;
+      gemm2::tc_gemm2_kernel<gemm::kTarget><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
+                                             ctx->stream>>>(ma, mb, mb, mo, p);
+    } else {
+      const int tiles = p.m_tiles * p.n_tiles;
+      const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+      gemm::tc_gemm_kernel<gemm::kTarget><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mb, mo,
+                                                                                                      mo, p);
+    }
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(Y);
@@ -453,17 +499,20 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
   const int64_t n = n_chunks_of(T, C);
   if (B == 0 || n == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
+    // pairs: 256-row tiles (each CTA loads 128 rows of the chunk's weight), whole tiles per chunk
+    const bool pairs = use_pairs(ctx) && C % gemm2::PAIR_M == 0;
+    const uint32_t w_rows = pairs ? gemm2::BN_HALF : gemm::BN;
     CUtensorMap ma, mb, mw0, mo;
-    if (!map_3d(ctx, &ma, Z, B, T, f, 128) || !map_3d(ctx, &mb, W_eff, B * n, d, f, 256) ||
+    if (!map_3d(ctx, &ma, Z, B, T, f, 128) || !map_3d(ctx, &mb, W_eff, B * n, d, f, w_rows) ||
         !map_3d(ctx, &mo, O, B, T, d, 32))
       return IPTTT_ERR_CUDA;
     if (W0 != nullptr) {
-      if (!map_2d(ctx, &mw0, W0, d, f, 64, 256)) return IPTTT_ERR_CUDA;
+      if (!map_2d(ctx, &mw0, W0, d, f, 64, w_rows)) return IPTTT_ERR_CUDA;
     } else {
       mw0 = mb;
     }
     gemm::Params p{};
-    p.m_tiles = (int)(C / gemm::BM);
+    p.m_tiles = (int)(C / (pairs ? gemm2::PAIR_M : gemm::BM));
     p.n_tiles = ceil_div(d, gemm::BN);
     p.k_blocks = ceil_div(f, gemm::BK);
     p.problems = (int)(B * n);
@@ -473,9 +522,15 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
     p.first_from_w0 = W0 != nullptr ? 1 : 0;
     p.st = dev_status(ctx);
     const int tiles = p.problems * p.m_tiles * p.n_tiles;
-    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-    gemm::tc_gemm_kernel<gemm::kApply><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mw0, mo, mo,
-                                                                                                   p);
+    if (pairs) {
+      p.group_m = 8;
+      gemm2::tc_gemm2_kernel<gemm::kApply><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
+                                            ctx->stream>>>(ma, mb, mw0, mo, p);
+    } else {
+      const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+      gemm::tc_gemm_kernel<gemm::kApply><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mw0, mo,
+                                                                                                     mo, p);
+    }
   } else {
     simt::SgemmParams p{};
     p.A = static_cast<const float*>(Z);
@@ -1105,6 +1160,12 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
 ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* stream) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
   ctx->stream = static_cast<cudaStream_t>(stream);
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_set_cta_pairs(ipttt_ctx* ctx, int enable) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ctx->cta_pairs = enable != 0;
   return IPTTT_OK;
 }
 

@@ -32,6 +32,7 @@ _SIGNATURES = {
     "ipttt_set_stream": (ctypes.c_int, [c_vp, c_vp]),
     "ipttt_set_wait_limit_ns": (ctypes.c_int, [c_vp, ctypes.c_uint64]),
     "ipttt_set_fused_tail": (ctypes.c_int, [c_vp, ctypes.c_int]),
+    "ipttt_set_cta_pairs": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_set_target_shift": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_sync": (ctypes.c_int, [c_vp]),
     "ipttt_last_error": (ctypes.c_char_p, [c_vp]),
@@ -180,6 +181,9 @@ class Context:
 
     def set_fused_tail(self, enable: bool):
         self._check(self.lib.ipttt_set_fused_tail(self.h, 1 if enable else 0), "set_fused_tail")
+
+    def set_cta_pairs(self, enable: bool):
+        self._check(self.lib.ipttt_set_cta_pairs(self.h, 1 if enable else 0), "set_cta_pairs")
 
     def set_wait_limit_ns(self, ns: int):
         self._check(self.lib.ipttt_set_wait_limit_ns(self.h, int(ns)), "set_wait_limit_ns")
