@@ -268,6 +268,7 @@ def run_ours(args, w):
     X0 = X_host.to(dev)
     ctx = pkg.Context(local)
     ctx.set_cta_pairs(not args.single_cta)
+    ctx.set_fused_tail(not args.unfused)
     stream = torch.cuda.current_stream(dev)
     O = torch.empty((w.B, w.T, w.d), dtype=H.dtype, device=dev)
     Wf = torch.empty((w.B, w.d, w.d_ff), dtype=torch.float32, device=dev)
@@ -546,7 +547,9 @@ def finish(args, w, ctx, stage_ms, timed_calls, launches, ms_max, world, clocks,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": workload_config(w) | {"parallelism": f"replicas x{world} (one sequence set per GPU)",
-                                            "gemm_tiles": "single CTA" if args.single_cta else "CTA pairs"},
+                                            "gemm_tiles": "single CTA" if args.single_cta else "CTA pairs",
+                                            "steps_3_5": "state kernel + apply GEMM" if args.unfused
+                                            else "fused state + apply kernel"},
             "tflops": layer_tflops, "frac_bf16_peak": layer_tflops / peaks["bf16_tflops"] / world,
             "frac_bf16_peak_sustained": layer_tflops / peaks["bf16_tflops_sustained"] / world,
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches * world if timed_calls == args.steps
@@ -612,6 +615,8 @@ def main(argv=None):
                          "d_ff in {0.5, 1, 4} x the workload's (the axes of the pages' ablations)")
     ap.add_argument("--single-cta", action="store_true",
                     help="run the bf16 GEMMs on single CTAs instead of CTA pairs (for comparison)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="run steps (3)-(5) as the state kernel and the apply GEMM instead of one fused kernel")
     ap.add_argument("--backward", action="store_true",
                     help="time the layer's backward pass instead (one GPU; its own JSON line)")
     args = ap.parse_args(argv)

@@ -81,3 +81,46 @@ def test_layer_pairs_match_single(ctx, fused, B, T, d, f, C, k):
     O_ref, W_ref = oracle.layer_forward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"],
                                         x["conv_w"], C, w.eta)
     assert rel_err(Oa, O_ref) <= TOL["bf16"] and rel_err(Wa, W_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("reverse_case", [False, True])
+@pytest.mark.parametrize("B,T,d,f,C", [(2, 300, 192, 384, 128), (1, 1024, 512, 1024, 256), (3, 130, 136, 264, 128),
+                                       (1, 5, 64, 64, 128)])
+def test_chunk_state_pairs_match_single(ctx, reverse_case, B, T, d, f, C):
+    """The state kernel on pairs (256-row units) and on single CTAs (128-row units); the reverse
+    scan is exercised through the backward pass."""
+    if not reverse_case:
+        V = seeded((B, T, d), 1.0, torch.bfloat16, 7, "cuda")
+        Z = seeded((B, T, f), C ** -0.5, torch.bfloat16, 8, "cuda")
+        W0 = seeded((d, f), 1.0, torch.bfloat16, 9, "cuda")
+        (Ea, Fa), (Eb, Fb) = both(ctx, lambda: tuple(t.clone() for t in ctx.chunk_state(V, Z, W0, C)))
+        assert torch.equal(Ea, Eb) and torch.equal(Fa, Fb)
+        for b in range(B):
+            ref_eff, ref_fin = oracle.chunk_weights(V[b].cpu(), Z[b].cpu(), W0.cpu(), C, 1.0)
+            assert rel_err(Fa[b], ref_fin) <= 1e-3 and rel_err(Ea[b], ref_eff) <= 1e-2
+    else:
+        w, x = random_case(B, T, d, f, C, 3, 2.0 / C, "bf16", 70 + T)
+        xd = to_dev(x)
+        dO = seeded((B, T, d), 1.0, torch.bfloat16, 71, "cuda")
+        dWf = seeded((B, d, f), 0.5, torch.float32, 72, "cuda")
+        ga, gb = both(ctx, lambda: {k: (None if v is None else v.clone()) for k, v in ctx.layer_backward(
+            xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"], xd["conv_w"], C, w.eta, dO,
+            dWf).items()})
+        for k in ga:
+            assert torch.equal(ga[k], gb[k]), k
+
+
+@pytest.mark.parametrize("B,T,d,f,C", [(2, 700, 256, 512, 256), (1, 600, 384, 768, 512)])
+def test_resume_pairs_match_single(ctx, B, T, d, f, C):
+    """The resumed layer (each sequence from its own fp32 state; the fused kernel then writes and
+    publishes W_eff[b, 0] itself) on pairs and on single CTAs, and against the oracle."""
+    w, x = random_case(B, T, d, f, C, 4, 2.0 / C, "bf16", 80 + T)
+    xd = to_dev(x)
+    W_state = (seeded((B, d, f), f ** -0.5, torch.float32, 81) + x["W_down0"].float()).cuda()
+    halo = seeded((B, 3, d), 0.02, torch.bfloat16, 82, "cuda")
+    (Oa, Wa, ha), (Ob, Wb, hb) = both(ctx, lambda: tuple(t.clone() for t in ctx.layer_resume(
+        xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], W_state, halo, C, w.eta)))
+    assert torch.equal(Oa, Ob) and torch.equal(Wa, Wb) and torch.equal(ha, hb)
+    O_ref, W_ref, _ = oracle.layer_resume(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_target"], x["conv_w"],
+                                          W_state.cpu(), halo.cpu(), C, w.eta)
+    assert rel_err(Oa, O_ref) <= TOL["bf16"] and rel_err(Wa, W_ref) <= TOL["bf16"]

@@ -17,9 +17,11 @@
 #include "ptx.cuh"
 #include "simt.cuh"
 #include "tc_fused.cuh"
+#include "tc_fused2.cuh"
 #include "tc_gemm.cuh"
 #include "tc_gemm2.cuh"
 #include "tc_state.cuh"
+#include "tc_state2.cuh"
 
 using namespace ipttt;
 
@@ -57,6 +59,7 @@ struct ipttt_ctx {
   bool fused_tail = true;  // run steps (3)-(5) as one cooperative kernel when possible
   bool cta_pairs = true;   // bf16 GEMMs on CTA pairs (cta_group::2) when the device allows
   int pair_ctas = 0;       // CTAs of the pair GEMM grid (2 x co-resident clusters; 0 = unavailable)
+  bool fused_pairs = true; // the cooperative launch of the fused pair kernel has not been refused
   int target_shift = 0;    // 1: the conv window of the target ends at the next token
   // The causal conv runs on an internal side stream, forked from and joined back into
   // `stream` with these events, so that it overlaps the SwiGLU GEMM.
@@ -271,17 +274,21 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
                            gemm::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (two-segment)");
   {
-    const void* pk[3] = {(const void*)gemm2::tc_gemm2_kernel<gemm::kSwiglu>,
+    const void* pk[5] = {(const void*)gemm2::tc_gemm2_kernel<gemm::kSwiglu>,
                          (const void*)gemm2::tc_gemm2_kernel<gemm::kTarget>,
-                         (const void*)gemm2::tc_gemm2_kernel<gemm::kApply>};
+                         (const void*)gemm2::tc_gemm2_kernel<gemm::kApply>, (const void*)state2::tc_state2_kernel,
+                         (const void*)fused2::tc_state_apply2_kernel};
+    const int pk_smem[5] = {gemm2::SMEM_BYTES, gemm2::SMEM_BYTES, gemm2::SMEM_BYTES, state2::SMEM_BYTES,
+                            fused2::SMEM_BYTES};
     int clusters = 1 << 30;
-    for (const void* k : pk) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm2::SMEM_BYTES);
-      if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (pair gemm)");
+    for (int ki = 0; ki < 5; ++ki) {
+      const void* k = pk[ki];
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pk_smem[ki]);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (pair kernels)");
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)(ctx->sm_count & ~1), 1, 1);
       cfg.blockDim = dim3(gemm2::NUM_THREADS, 1, 1);
-      cfg.dynamicSmemBytes = gemm2::SMEM_BYTES;
+      cfg.dynamicSmemBytes = pk_smem[ki];
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
         cudaGetLastError();
@@ -436,6 +443,23 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
   return check_launch(ctx, "target launch");
 }
 
+// The bf16 state kernel on CTA pairs (256-row units) or single CTAs (128-row units); p's
+// m_units / units are given for 128-row units and recomputed here for pairs.
+ipttt_status launch_state_kernel(ipttt_ctx* ctx, const CUtensorMap& mv, const CUtensorMap& mz, const CUtensorMap& mw,
+                                 const CUtensorMap& mf, state::Params p) {
+  if (use_pairs(ctx)) {
+    p.m_units = ceil_div(p.d, state2::PAIR_D);
+    p.units = p.B * p.m_units * p.n_units;
+    state2::tc_state2_kernel<<<pair_grid(ctx, (p.units + 1) / 2), state2::NUM_THREADS, state2::SMEM_BYTES,
+                               ctx->stream>>>(mv, mz, mw, mf, p);
+  } else {
+    const int pairs = (p.units + 1) / 2;
+    const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
+    state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, mw, mf, p);
+  }
+  return check_launch(ctx, "state launch");
+}
+
 // Steps (3)+(4).  fp32: Step 1 (all Delta_i) then Step 2 (scan); bf16: one fused kernel.
 // skip_first (bf16): leave W_eff[b, 0] (= W_down0) unwritten; the layer's apply then reads
 // W_down0 for chunk 0 directly.
@@ -464,10 +488,7 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
     p.skip_first = (skip_first && W_init == nullptr) ? 1 : 0;
     p.W_init = W_init;
     p.st = dev_status(ctx);
-    const int pairs = (p.units + 1) / 2;
-    const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
-    state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, mw, mf, p);
-    return check_launch(ctx, "state launch");
+    return launch_state_kernel(ctx, mv, mz, mw, mf, p);
   }
   simt::SgemmParams p{};
   p.A = static_cast<const float*>(V);
@@ -553,9 +574,78 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
 
 // Steps (3)-(5) as one cooperative kernel: state unit pairs, then apply tiles from a queue
 // (tc_fused.cuh).  `ctr` holds B*n slice counters and the queue head, zeroed beforehand.
+// The pair version (tc_fused2.cuh): 256-row state units and apply tiles (C % 256 == 0).
+// Returns false, having launched nothing, when the cooperative cluster launch is refused.
+bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
+                              int64_t d, int64_t f, int64_t C, void* W_eff, float* W_final, void* O, uint32_t* ctr,
+                              const float* W_init, ipttt_status* st) {
+  const int64_t n = n_chunks_of(T, C);
+  CUtensorMap mv, mz, mw_st, mf, mza, mw_ld, mw0, mo;
+  *st = IPTTT_ERR_CUDA;
+  if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64) ||
+      !map_3d(ctx, &mw_st, W_eff, B * n, d, f, 32) || !map_3d_f32(ctx, &mf, W_final, B, d, f, 32) ||
+      !map_3d(ctx, &mza, Z, B, T, f, 128) || !map_3d(ctx, &mw_ld, W_eff, B * n, d, f, 128) ||
+      !map_3d(ctx, &mo, O, B, T, d, 32))
+    return true;
+  if (W_init == nullptr) {
+    if (!map_2d(ctx, &mw0, W0, d, f, 64, 128)) return true;
+  } else {
+    mw0 = mw_ld;  // unused: chunk 0 reads W_eff[b, 0]
+  }
+  fused::Params p{};
+  p.s.B = (int)B;
+  p.s.T = (int)T;
+  p.s.d = (int)d;
+  p.s.f = (int)f;
+  p.s.C = (int)C;
+  p.s.n_chunks = (int)n;
+  p.s.m_units = ceil_div(d, state2::PAIR_D);
+  p.s.n_units = ceil_div(f, state2::BNF);
+  p.s.units = (int)(B * p.s.m_units * p.s.n_units);
+  p.s.W0 = static_cast<const __nv_bfloat16*>(W0);
+  p.s.skip_first = W_init == nullptr ? 1 : 0;
+  p.s.W_init = W_init;
+  p.s.st = dev_status(ctx);
+  p.a.m_tiles = (int)(C / gemm2::PAIR_M);
+  p.a.n_tiles = ceil_div(d, gemm2::BN);
+  p.a.k_blocks = ceil_div(f, gemm2::BK);
+  p.a.problems = (int)(B * n);
+  p.a.group_m = 8;
+  p.a.scale = 1.f;
+  p.a.T = (int)T, p.a.C = (int)C, p.a.n_chunks = (int)n;
+  p.a.first_from_w0 = p.s.skip_first;
+  p.a.st = dev_status(ctx);
+  p.ready = ctr;
+  p.next_tile = ctr + B * n;
+  p.ready_target = (uint32_t)(p.s.m_units * p.s.n_units * 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctx->pair_ctas);
+  cfg.blockDim = dim3(fused2::NUM_THREADS);
+  cfg.dynamicSmemBytes = fused2::SMEM_BYTES;
+  cfg.stream = ctx->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, fused2::tc_state_apply2_kernel, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // a refused launch configuration is not sticky
+    ctx->fused_pairs = false;
+    return false;
+  }
+  *st = check_launch(ctx, "state+apply launch");
+  return true;
+}
+
 ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
                                    int64_t d, int64_t f, int64_t C, void* W_eff, float* W_final, void* O,
                                    uint32_t* ctr, const float* W_init = nullptr) {
+  if (use_pairs(ctx) && ctx->fused_pairs && C % gemm2::PAIR_M == 0) {
+    ipttt_status st;
+    if (launch_state_apply_pairs(ctx, V, Z, W0, B, T, d, f, C, W_eff, W_final, O, ctr, W_init, &st)) return st;
+  }
   const int64_t n = n_chunks_of(T, C);
   CUtensorMap mv, mz, mw_st, mf, mza, mw_ld, mw0, mo;
   if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64) ||
@@ -644,10 +734,7 @@ ipttt_status launch_state_general(ipttt_ctx* ctx, const void* V, int64_t v_strid
   p.W_init = W_init;
   p.reverse = reverse ? 1 : 0;
   p.st = dev_status(ctx);
-  const int pairs = (p.units + 1) / 2;
-  const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
-  state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, mw, mf, p);
-  return check_launch(ctx, "state launch");
+  return launch_state_kernel(ctx, mv, mz, mw, mf, p);
 }
 
 // C = A1 B1 + A2 B2 (bf16, kTwoSeg): A segments token-major [B, T, K] (a2 = A1's map shifted by
