@@ -274,14 +274,16 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
                            gemm::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (two-segment)");
   {
-    const void* pk[5] = {(const void*)gemm2::tc_gemm2_kernel<gemm::kSwiglu>,
+    const void* pk[7] = {(const void*)gemm2::tc_gemm2_kernel<gemm::kSwiglu>,
                          (const void*)gemm2::tc_gemm2_kernel<gemm::kTarget>,
-                         (const void*)gemm2::tc_gemm2_kernel<gemm::kApply>, (const void*)state2::tc_state2_kernel,
+                         (const void*)gemm2::tc_gemm2_kernel<gemm::kApply>,
+                         (const void*)gemm2::tc_gemm2_kernel<gemm::kSwigluSave>,
+                         (const void*)gemm2::tc_gemm2_kernel<gemm::kTwoSeg>, (const void*)state2::tc_state2_kernel,
                          (const void*)fused2::tc_state_apply2_kernel};
-    const int pk_smem[5] = {gemm2::SMEM_BYTES, gemm2::SMEM_BYTES, gemm2::SMEM_BYTES, state2::SMEM_BYTES,
-                            fused2::SMEM_BYTES};
+    const int pk_smem[7] = {gemm2::SMEM_BYTES, gemm2::SMEM_BYTES, gemm2::SMEM_BYTES, gemm2::SMEM_BYTES,
+                            gemm2::SMEM_BYTES, state2::SMEM_BYTES, fused2::SMEM_BYTES};
     int clusters = 1 << 30;
-    for (int ki = 0; ki < 5; ++ki) {
+    for (int ki = 0; ki < 7; ++ki) {
       const void* k = pk[ki];
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pk_smem[ki]);
       if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (pair kernels)");
@@ -341,7 +343,7 @@ ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const voi
     const int tiles = p.m_tiles * p.n_tiles;
     if (pairs) {
       gemm2::tc_gemm2_kernel<gemm::kSwiglu><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
-                                             ctx->stream>>>(ma, mb0, mb1, mo, p);
+                                             ctx->stream>>>(ma, mb0, mb1, mo, mo, p);
     } else {
       const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
       gemm::tc_gemm_kernel<gemm::kSwiglu><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb0, mb1,
@@ -420,7 +422,7 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
       p.group_m = 8;
       const int tiles = p.m_tiles * p.n_tiles;
       gemm2::tc_gemm2_kernel<gemm::kTarget><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
-                                             ctx->stream>>>(ma, mb, mb, mo, p);
+                                             ctx->stream>>>(ma, mb, mb, mo, mo, p);
     } else {
       const int tiles = p.m_tiles * p.n_tiles;
       const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
@@ -546,7 +548,7 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
     if (pairs) {
       p.group_m = 8;
       gemm2::tc_gemm2_kernel<gemm::kApply><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
-                                            ctx->stream>>>(ma, mb, mw0, mo, p);
+                                            ctx->stream>>>(ma, mb, mw0, mo, mo, p);
     } else {
       const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
       gemm::tc_gemm_kernel<gemm::kApply><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma, mb, mw0, mo,
@@ -760,8 +762,9 @@ ipttt_status launch_two_seg(ipttt_ctx* ctx, const void* A1, int64_t a1_stride, c
   } else {
     mo = ma1;  // never stored through
   }
+  const bool pairs = use_pairs(ctx) && C % gemm2::PAIR_M == 0;
   gemm::Params p{};
-  p.m_tiles = (int)(C / gemm::BM);
+  p.m_tiles = (int)(C / (pairs ? gemm2::PAIR_M : gemm::BM));
   p.n_tiles = ceil_div(N, gemm::BN);
   p.k_blocks = ceil_div(K1, gemm::BK);
   p.k_blocks2 = ceil_div(K2, gemm::BK);
@@ -775,9 +778,15 @@ ipttt_status launch_two_seg(ipttt_ctx* ctx, const void* A1, int64_t a1_stride, c
   p.T = (int)T, p.C = (int)C, p.n_chunks = (int)n;
   p.st = dev_status(ctx);
   const int tiles = p.problems * p.m_tiles * p.n_tiles;
-  const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-  gemm::tc_gemm_kernel<gemm::kTwoSeg><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma1, mb1, ma2, mo,
-                                                                                                    mb2, p);
+  if (pairs) {
+    p.group_m = 8;
+    gemm2::tc_gemm2_kernel<gemm::kTwoSeg><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
+                                           ctx->stream>>>(ma1, mb1, ma2, mo, mb2, p);
+  } else {
+    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+    gemm::tc_gemm_kernel<gemm::kTwoSeg><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(ma1, mb1, ma2,
+                                                                                                      mo, mb2, p);
+  }
   return check_launch(ctx, "two-segment launch");
 }
 
@@ -852,7 +861,7 @@ ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const v
   float* part = reinterpret_cast<float*>(base + L.part);
   const int64_t n = n_chunks_of(T, C);
   const int64_t BT = B * T;
-  const int64_t CT = (BT + 127) / 128 * 128;  // all tokens as one chunk (flat GEMMs and reductions)
+  const int64_t CT = (BT + 255) / 256 * 256;  // all tokens as one chunk (flat GEMMs and reductions)
   const bool bf16 = dt == IPTTT_BF16;
   const int64_t df = d * f;
   if (bf16) {
@@ -868,18 +877,24 @@ ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const v
           !map_2d(ctx, &mb1, Wu, f, d, 64, 128) || !map_2d(ctx, &mo, Z, BT, f, 64, 32) ||
           !encode_map(ctx, &mx, AU, 3, au_dims, au_strides, au_box))
         return IPTTT_ERR_CUDA;
+      const bool pairs = use_pairs(ctx);
       gemm::Params p{};
-      p.m_tiles = ceil_div(BT, gemm::BM);
+      p.m_tiles = ceil_div(BT, pairs ? gemm2::PAIR_M : gemm::BM);
       p.n_tiles = ceil_div(f, 128);
       p.k_blocks = ceil_div(d, gemm::BK);
       p.problems = 1;
-      p.group_m = 16;
+      p.group_m = pairs ? 8 : 16;
       p.scale = 1.f;
       p.st = dev_status(ctx);
       const int tiles = p.m_tiles * p.n_tiles;
-      const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-      gemm::tc_gemm_kernel<gemm::kSwigluSave><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(
-          ma, mb0, mb1, mo, mx, p);
+      if (pairs) {
+        gemm2::tc_gemm2_kernel<gemm::kSwigluSave><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
+                                                   ctx->stream>>>(ma, mb0, mb1, mo, mx, p);
+      } else {
+        const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+        gemm::tc_gemm_kernel<gemm::kSwigluSave><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(
+            ma, mb0, mb1, mo, mx, p);
+      }
       if ((s = check_launch(ctx, "swiglu save launch")) != IPTTT_OK) return s;
     }
   } else {

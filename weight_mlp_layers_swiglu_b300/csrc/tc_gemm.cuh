@@ -87,6 +87,43 @@ __device__ __forceinline__ bool tile_active(const Params& p, int prob, int mt) {
   return true;
 }
 
+// The SwiGLU adjoint for 64 columns n0.. of one token's row: dZ (fp32) in lo/hi, A and U read
+// from au_row = [A | U] (bf16, au_f columns each) and overwritten with dA and dU:
+// dA = dZ U s (1 + A (1 - s)), dU = dZ A s, s = sigmoid(A).  d_ff % 8 == 0, so each group of 8
+// columns lies wholly inside or outside the row.
+__device__ __forceinline__ void swiglu_adjoint_row64(const uint32_t (&lo)[32], const uint32_t (&hi)[32],
+                                                     __nv_bfloat16* au_row, int n0, int au_f) {
+  uint4 av[8], uv[8];
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    if (n0 + v * 8 < au_f) {
+      av[v] = *reinterpret_cast<const uint4*>(au_row + n0 + v * 8);
+      uv[v] = *reinterpret_cast<const uint4*>(au_row + au_f + n0 + v * 8);
+    }
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    if (n0 + v * 8 >= au_f) continue;
+    const uint32_t* aw = reinterpret_cast<const uint32_t*>(&av[v]);
+    const uint32_t* uw = reinterpret_cast<const uint32_t*>(&uv[v]);
+    uint4 da, du;
+    uint32_t* daw = reinterpret_cast<uint32_t*>(&da);
+    uint32_t* duw = reinterpret_cast<uint32_t*>(&du);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = (v & 3) * 8 + 2 * e;
+      const float z0 = __uint_as_float(v < 4 ? lo[j] : hi[j]);
+      const float z1 = __uint_as_float(v < 4 ? lo[j + 1] : hi[j + 1]);
+      const float A0 = bf16_lo(aw[e]), A1 = bf16_hi(aw[e]);
+      const float U0 = bf16_lo(uw[e]), U1 = bf16_hi(uw[e]);
+      const float s0 = 1.0f / (1.0f + __expf(-A0)), s1 = 1.0f / (1.0f + __expf(-A1));
+      daw[e] = pack_bf16x2(z0 * U0 * s0 * (1.0f + A0 * (1.0f - s0)), z1 * U1 * s1 * (1.0f + A1 * (1.0f - s1)));
+      duw[e] = pack_bf16x2(z0 * A0 * s0, z1 * A1 * s1);
+    }
+    *reinterpret_cast<uint4*>(au_row + n0 + v * 8) = da;
+    *reinterpret_cast<uint4*>(au_row + au_f + n0 + v * 8) = du;
+  }
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
@@ -301,43 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait(lo);
           tmem_ld_wait(hi);
           const int n0 = nt * BN + h * 64;
-          if (tok < p.T) {
-            // 8 groups of 8 columns; d_ff % 8 == 0, so a group lies wholly inside or outside
-            uint4 av[8], uv[8];
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              if (n0 + v * 8 < p.au_f) {
-                av[v] = *reinterpret_cast<const uint4*>(au_row + n0 + v * 8);
-                uv[v] = *reinterpret_cast<const uint4*>(au_row + p.au_f + n0 + v * 8);
-              }
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              if (n0 + v * 8 >= p.au_f) continue;
-              const uint32_t* aw = reinterpret_cast<const uint32_t*>(&av[v]);
-              const uint32_t* uw = reinterpret_cast<const uint32_t*>(&uv[v]);
-              uint4 da, du;
-              uint32_t* daw = reinterpret_cast<uint32_t*>(&da);
-              uint32_t* duw = reinterpret_cast<uint32_t*>(&du);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float ga[2], gd[2];
-                const float A0 = bf16_lo(aw[e]), A1 = bf16_hi(aw[e]);
-                const float U0 = bf16_lo(uw[e]), U1 = bf16_hi(uw[e]);
-                const int j = (v & 3) * 8 + 2 * e;
-                const float z0 = __uint_as_float(v < 4 ? lo[j] : hi[j]);
-                const float z1 = __uint_as_float(v < 4 ? lo[j + 1] : hi[j + 1]);
-                const float s0 = 1.0f / (1.0f + __expf(-A0)), s1 = 1.0f / (1.0f + __expf(-A1));
-                ga[0] = z0 * U0 * s0 * (1.0f + A0 * (1.0f - s0));
-                ga[1] = z1 * U1 * s1 * (1.0f + A1 * (1.0f - s1));
-                gd[0] = z0 * A0 * s0;
-                gd[1] = z1 * A1 * s1;
-                daw[e] = pack_bf16x2(ga[0], ga[1]);
-                duw[e] = pack_bf16x2(gd[0], gd[1]);
-              }
-              *reinterpret_cast<uint4*>(au_row + n0 + v * 8) = da;
-              *reinterpret_cast<uint4*>(au_row + p.au_f + n0 + v * 8) = du;
-            }
-          }
+          if (tok < p.T) swiglu_adjoint_row64(lo, hi, au_row, n0, p.au_f);
         }
       } else {
 #pragma unroll 1

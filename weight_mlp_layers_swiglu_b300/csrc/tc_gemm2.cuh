@@ -14,9 +14,13 @@
 //               buffer is released to the MMA issuer once both CTAs' epilogues have read it.
 //
 // Steps served (zhichai.net "In-Place TTT：给LLM装上"临时记忆插槽"，让它边读边学"):
-//   kSwiglu  §3.1 gated MLP; B half 0 = 128 rows of W_gate, half 1 = the same rows of W_up.
-//   kTarget  §3.3 target projection (B = W_target, MN-major).
-//   kApply   §3.2 Step 3 per chunk (requires C % 256 == 0 so a pair tile never spans chunks).
+//   kSwiglu      §3.1 gated MLP; B half 0 = 128 rows of W_gate, half 1 = the same rows of W_up.
+//   kTarget      §3.3 target projection (B = W_target, MN-major).
+//   kApply       §3.2 Step 3 per chunk (requires C % 256 == 0 so a pair tile never spans chunks).
+//   kSwigluSave  kSwiglu that also stores [A | U] through map_x ([rows][2][d_ff]), for the
+//                backward pass.
+//   kTwoSeg      the backward pass's A1 B1 + A2 B2 (B operands MN-major), per chunk like kApply,
+//                with the optional SwiGLU-adjoint epilogue of tc_gemm.cuh (p.au).
 #pragma once
 
 #include "tc_gemm.cuh"
@@ -27,7 +31,9 @@ namespace gemm2 {
 using gemm::Kind;
 using gemm::kApply;
 using gemm::kSwiglu;
+using gemm::kSwigluSave;
 using gemm::kTarget;
+using gemm::kTwoSeg;
 using gemm::Params;
 
 constexpr int BM = 128;        // rows per CTA (the pair tile has 256)
@@ -49,7 +55,7 @@ static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier block");
 
 template <int KIND>
 __device__ __forceinline__ bool pair_tile_active(const Params& p, int prob, int mt) {
-  if (KIND == kApply) {
+  if (KIND == kApply || KIND == kTwoSeg) {
     const int i = prob % p.n_chunks;
     return i * p.C + mt * PAIR_M < p.T;
   }
@@ -60,7 +66,7 @@ template <int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tc_gemm2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                     const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_out,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap map_x, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_stage = smem + STAGES * STAGE_BYTES;
@@ -79,6 +85,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int pair = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
   const int total_tiles = p.problems * p.m_tiles * p.n_tiles;
+  const int k_total = p.k_blocks + (KIND == kTwoSeg ? p.k_blocks2 : 0);
 
   if (p.zero_ptr != nullptr && blockIdx.x == 0)
     for (int i = threadIdx.x; i < p.zero_count; i += blockDim.x) p.zero_ptr[i] = 0u;
@@ -113,13 +120,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b0);
     if (KIND != kTarget) tma_prefetch_desc(&map_b1);
+    if (KIND == kTwoSeg) tma_prefetch_desc(&map_x);
     for (int tile = pair; tile < total_tiles; tile += n_pairs) {
       int prob, mt, nt;
       gemm::decode_tile(p, tile, prob, mt, nt);
       if (!pair_tile_active<KIND>(p, prob, mt)) continue;
       const int m0 = mt * PAIR_M + (int)rank * BM;
       bool ok = true;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
+      for (int kb = 0; kb < k_total; ++kb) {
         if (!wait_bounded(&empty[p_stage], p_phase ^ 1u, p.st, abort_flag, 0x501)) {
           ok = false;
           break;
@@ -129,9 +137,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t bar = cluster_addr(smem_u32(&full[p_stage]), 0);
         if (rank == 0) mbar_arrive_expect_tx(&full[p_stage], 2 * STAGE_BYTES);
         const int k0 = kb * BK;
-        if (KIND == kSwiglu) {
+        if (KIND == kSwiglu || KIND == kSwigluSave) {
           tma_load_2d_pair(sa, &map_a, bar, k0, m0);
           tma_load_2d_pair(sb, rank == 0 ? &map_b0 : &map_b1, bar, k0, nt * BN_HALF);
+        } else if (KIND == kTwoSeg) {
+          const int b = prob / p.n_chunks;
+          const int i = prob - b * p.n_chunks;
+          const bool second = kb >= p.k_blocks;
+          const int kk0 = second ? (kb - p.k_blocks) * BK : k0;
+          const int bslice = p.b_per_problem ? prob : 0;
+          tma_load_3d_pair(sa, second ? &map_b1 : &map_a, bar, kk0 + (second ? p.a2_koff : 0), i * p.C + m0, b);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load_3d_pair(sb + j * (BK * 128), second ? &map_x : &map_b0, bar,
+                             nt * BN + (int)rank * BN_HALF + j * 64, kk0, bslice);
         } else if (KIND == kTarget) {
           tma_load_2d_pair(sa, &map_a, bar, k0, m0);
 #pragma unroll
@@ -155,7 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
-    constexpr bool b_mn = KIND == kTarget;
+    constexpr bool b_mn = KIND == kTarget || KIND == kTwoSeg;
     constexpr uint32_t idesc = idesc_bf16(PAIR_M, BN, false, b_mn);
     int stage = 0;
     uint32_t phase = 0;
@@ -170,7 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
       bool ok = true;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
+      for (int kb = 0; kb < k_total; ++kb) {
         if (!wait_bounded(&full[stage], phase, p.st, abort_flag, 0x503)) {
           ok = false;
           break;
@@ -210,7 +229,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
       const int row0 = mt * PAIR_M + (int)rank * BM + q * 32;
-      if (KIND == kSwiglu) {
+      if (KIND == kSwiglu || KIND == kSwigluSave) {
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           uint32_t row[32];
@@ -230,6 +249,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             }
           }
           out.put(row, &map_out, nt * BN_HALF + h * 64, row0);
+          if (KIND == kSwigluSave) {  // the gate and up pre-activations: map_x is [rows][2][d_ff]
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part) {
+              uint32_t pre[32];
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                uint32_t g[32];
+                tmem_ld32(t_row + part * BN_HALF + h * 64 + c * 32, g);
+                tmem_ld_wait(g);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  pre[c * 16 + e] = pack_bf16x2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1]));
+              }
+              out.put(pre, &map_x, nt * BN_HALF + h * 64, part, row0);
+            }
+          }
+        }
+      } else if (KIND == kTwoSeg && p.au != nullptr) {
+        // dZ stays in registers: the SwiGLU adjoints overwrite [A | U] in place (tc_gemm.cuh)
+        const int bq = prob / p.n_chunks;
+        const int i = prob - bq * p.n_chunks;
+        const int tok = i * p.C + row0 + lane;
+        __nv_bfloat16* au_row = p.au + ((int64_t)bq * p.T + tok) * (2 * (int64_t)p.au_f);
+#pragma unroll 1
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t lo[32], hi[32];
+          tmem_ld32(t_row + h * 64, lo);
+          tmem_ld32(t_row + h * 64 + 32, hi);
+          tmem_ld_wait(lo);
+          tmem_ld_wait(hi);
+          const int n0 = nt * BN + h * 64;
+          if (tok < p.T) gemm::swiglu_adjoint_row64(lo, hi, au_row, n0, p.au_f);
         }
       } else {
 #pragma unroll 1
@@ -244,7 +295,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             row[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
             row[16 + e] = pack_bf16x2(__uint_as_float(b[2 * e]) * p.scale, __uint_as_float(b[2 * e + 1]) * p.scale);
           }
-          if (KIND == kApply) {
+          if (KIND == kApply || KIND == kTwoSeg) {
             const int bq = prob / p.n_chunks;
             const int i = prob - bq * p.n_chunks;
             out.put(row, &map_out, nt * BN + h * 64, i * p.C + row0, bq);
