@@ -171,15 +171,21 @@ ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const voi
                                         ipttt_dtype dtype, void* O, float* W_state_out, void* X0_halo_out,
                                         void* workspace, size_t workspace_bytes);
 
-/* Bytes of device workspace ipttt_layer_forward_host needs: ipttt_workspace_size() plus
- * device staging for H, X0, O and W_final. */
+/* Bytes of device workspace ipttt_layer_forward_host needs: ipttt_workspace_size() for one
+ * piece (see below), then device staging for the whole H, X0 and O, the fp32 state [B,d,d_ff]
+ * and two conv halos [B,k-1,d]. */
 ipttt_status ipttt_host_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
                                        ipttt_dtype dtype, size_t* bytes);
 
 /* The whole layer with the activations and results in HOST memory (pinned memory gives
- * asynchronous copies): H_host, X0_host [B,T,d] dtype are copied to the device, the layer
- * runs, O_host [B,T,d] dtype and W_final_host [B,d,d_ff] fp32 are copied back, all in order
- * on the context's stream.  The frozen weights stay device pointers.  The host buffers
+ * asynchronous copies): H_host, X0_host [B,T,d] dtype in, O_host [B,T,d] dtype and
+ * W_final_host [B,d,d_ff] fp32 out; the frozen weights stay device pointers.  The call runs in
+ * pieces of about 4096 tokens (a multiple of C, at most 64 pieces): piece j is uploaded on an
+ * internal copy stream, computed on the context's stream as a resumed call (the state and conv
+ * halo of piece j-1), and its O downloaded on a second copy stream, so the copies of one piece
+ * overlap the compute of its neighbours.  Pieces start at multiples of C, so the results equal
+ * ipttt_layer_forward's bit for bit.  Everything is ordered after the work already on the
+ * context's stream, and the context's stream waits for all of it at the end: the host buffers
  * must stay valid until ipttt_sync() returns.  Errors as ipttt_layer_forward. */
 ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const void* X0_host,
                                       const void* W_gate, const void* W_up, const void* W_down0,

@@ -102,8 +102,17 @@ def test_deterministic(ctx):
     assert torch.equal(O1, O2) and torch.equal(W1, W2)
 
 
-def test_host_buffer_entry_point_matches(ctx):
-    w, x = random_case(2, 384, 256, 512, 128, 4, 1.0 / 128, "bf16", 6)
+@pytest.mark.parametrize("dt,B,T,d,f,C,k", [
+    ("bf16", 2, 384, 256, 512, 128, 4),     # one piece
+    ("bf16", 2, 9000, 256, 512, 1024, 4),   # three pieces (4096, 4096, 808): uploads, compute and downloads overlap
+    ("bf16", 1, 12288, 128, 256, 512, 1),   # three whole pieces, no conv halo
+    ("f32", 2, 5000, 64, 128, 48, 3),       # pieces of 4128 tokens
+])
+def test_host_buffer_entry_point_matches(ctx, dt, B, T, d, f, C, k):
+    """The host-buffer entry runs a call in pieces (multiples of C) whose copies overlap the
+    compute; each piece resumes from the previous one's state and halo, so the result is the
+    device entry's bit for bit."""
+    w, x = random_case(B, T, d, f, C, k, 1.0 / C, dt, 6)
     O, Wf = run(ctx, w, x)
     xd = to_dev(x)
     H_h, X_h = x["H"].pin_memory(), x["X0"].pin_memory()

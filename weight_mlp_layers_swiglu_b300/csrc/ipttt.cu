@@ -32,6 +32,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 namespace {
 
 constexpr int kMaxTimedCalls = 256;
+constexpr int kMaxPieces = 64;           // pieces of one host-buffer call
+constexpr int64_t kPieceTokens = 4096;   // target piece length (rounded up to a multiple of C)
 // Timing events recorded per timed layer call.
 enum : int {
   kEvStart = 0,       // context stream, before the fork
@@ -65,6 +67,11 @@ struct ipttt_ctx {
   // `stream` with these events, so that it overlaps the SwiGLU GEMM.
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  // The host-buffer entry pipelines pieces of a call: uploads on copy_in and downloads on
+  // copy_out overlap the compute on `stream` (per-piece events in piece_ev).
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t h_fork = nullptr, h_join = nullptr;
+  std::vector<cudaEvent_t> piece_ev;  // [2 * kMaxPieces]: upload done, compute done
   // timing
   bool timing = false;
   int timed_calls = 0;
@@ -840,6 +847,41 @@ BwdLayout bwd_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, int 
   return L;
 }
 
+// Pieces of a host-buffer call: a multiple of C near kPieceTokens, at most kMaxPieces of them.
+int64_t piece_len(int64_t T, int64_t C) {
+  int64_t P = (kPieceTokens + C - 1) / C * C;
+  const int64_t min_p = ((T + kMaxPieces - 1) / kMaxPieces + C - 1) / C * C;
+  if (P < min_p) P = min_p;
+  return P < T ? P : T;
+}
+
+// Device workspace of the host-buffer entry: the layer's workspace for one piece, then H, X0
+// and O staged whole (piece j at offset B * lo * d), the fp32 state and two conv halos.
+struct HostLayout {
+  size_t h, x, o, w, halo0, halo1, total;
+  int64_t piece;
+};
+
+HostLayout host_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, int k, ipttt_dtype dt) {
+  const size_t es = esize(dt);
+  HostLayout L;
+  L.piece = piece_len(T, C);
+  size_t off = ws_layout(B, L.piece, d, f, C, dt).total;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  L.h = take((size_t)B * T * d * es);
+  L.x = take((size_t)B * T * d * es);
+  L.o = take((size_t)B * T * d * es);
+  L.w = take((size_t)B * d * f * 4);
+  L.halo0 = take((size_t)B * (k - 1) * d * es);
+  L.halo1 = take((size_t)B * (k - 1) * d * es);
+  L.total = off;
+  return L;
+}
+
 // The backward pass (validated by the caller; T >= 1).
 ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
                           const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d, int64_t f,
@@ -1243,9 +1285,21 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
   }
   if (cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&ctx->fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ctx->join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventCreateWithFlags(&ctx->join, cudaEventDisableTiming) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&ctx->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&ctx->copy_out, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->h_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->h_join, cudaEventDisableTiming) != cudaSuccess) {
     ipttt_destroy(ctx);
     return IPTTT_ERR_CUDA;
+  }
+  ctx->piece_ev.assign(2 * kMaxPieces, nullptr);
+  for (auto& e : ctx->piece_ev) {
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      e = nullptr;
+      ipttt_destroy(ctx);
+      return IPTTT_ERR_CUDA;
+    }
   }
   ctx->events.resize((size_t)kMaxTimedCalls * kEventsPerCall, nullptr);
   ctx->timed_fused.assign(kMaxTimedCalls, 0);
@@ -1327,6 +1381,12 @@ void ipttt_destroy(ipttt_ctx* ctx) {
   if (ctx->fork) cudaEventDestroy(ctx->fork);
   if (ctx->join) cudaEventDestroy(ctx->join);
   if (ctx->side) cudaStreamDestroy(ctx->side);
+  for (auto& e : ctx->piece_ev)
+    if (e) cudaEventDestroy(e);
+  if (ctx->h_fork) cudaEventDestroy(ctx->h_fork);
+  if (ctx->h_join) cudaEventDestroy(ctx->h_join);
+  if (ctx->copy_in) cudaStreamDestroy(ctx->copy_in);
+  if (ctx->copy_out) cudaStreamDestroy(ctx->copy_out);
   if (ctx->status) cudaFree(ctx->status);
   delete ctx;
 }
@@ -1345,9 +1405,7 @@ ipttt_status ipttt_host_workspace_size(int64_t B, int64_t T, int64_t d, int64_t 
   if (!bytes) return IPTTT_ERR_INVALID_ARG;
   const ipttt_status s = check_shape(nullptr, B, T, d, d_ff, C, k, dt);
   if (s != IPTTT_OK) return s;
-  const size_t es = esize(dt);
-  const size_t act = align256((size_t)B * T * d * es);
-  *bytes = ws_layout(B, T, d, d_ff, C, dt).total + 3 * act + align256((size_t)B * d * d_ff * 4);
+  *bytes = host_layout(B, T, d, d_ff, C, k, dt).total;
   return IPTTT_OK;
 }
 
@@ -1538,31 +1596,72 @@ ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const 
     return IPTTT_ERR_INVALID_ARG;
   }
   const size_t es = esize(dt);
-  const size_t act = (size_t)B * T * d * es;
-  const size_t layer_ws = ws_layout(B, T, d, d_ff, C, dt).total;
+  const HostLayout HL = host_layout(B, T, d, d_ff, C, k, dt);
+  const int64_t P = HL.piece;
+  const size_t layer_ws = ws_layout(B, P, d, d_ff, C, dt).total;
   uint8_t* base = static_cast<uint8_t*>(ws);
-  void* Hd = base + layer_ws;
-  void* Xd = base + layer_ws + align256(act);
-  void* Od = base + layer_ws + 2 * align256(act);
-  float* Wfd = reinterpret_cast<float*>(base + layer_ws + 3 * align256(act));
-  s = validate_layer(ctx, T > 0 ? Hd : nullptr, T > 0 ? Xd : nullptr, W_gate, W_up, W_down0, W_target, conv_w, B, T,
-                     d, d_ff, C, k, eta, dt, T > 0 ? Od : nullptr, Wfd, ws, layer_ws, false);
+  uint8_t* Hd = base + HL.h;
+  uint8_t* Xd = base + HL.x;
+  uint8_t* Od = base + HL.o;
+  float* Wst = reinterpret_cast<float*>(base + HL.w);
+  void* halo[2] = {base + HL.halo0, base + HL.halo1};
+  s = validate_layer(ctx, P > 0 ? Hd : nullptr, P > 0 ? Xd : nullptr, W_gate, W_up, W_down0, W_target, conv_w, B, P, d,
+                     d_ff, C, k, eta, dt, P > 0 ? Od : nullptr, Wst, ws, layer_ws, false);
   if (s != IPTTT_OK) return s;
   DeviceGuard g(ctx->device);
   cudaError_t e;
-  if (T > 0) {
-    if ((e = cudaMemcpyAsync(Hd, H_host, act, cudaMemcpyHostToDevice, ctx->stream)) != cudaSuccess)
-      return cuda_fail(ctx, e, "H upload");
-    if ((e = cudaMemcpyAsync(Xd, X0_host, act, cudaMemcpyHostToDevice, ctx->stream)) != cudaSuccess)
-      return cuda_fail(ctx, e, "X0 upload");
+  const size_t state_bytes = (size_t)B * d * d_ff * 4;
+  if (T == 0) {  // W_final[b] = W_down0
+    if ((s = run_layer(ctx, nullptr, nullptr, W_gate, W_up, W_down0, W_target, conv_w, B, 0, d, d_ff, C, k, eta, dt,
+                       nullptr, Wst, ws)) != IPTTT_OK)
+      return s;
+    if ((e = cudaMemcpyAsync(W_final_host, Wst, state_bytes, cudaMemcpyDeviceToHost, ctx->stream)) != cudaSuccess)
+      return cuda_fail(ctx, e, "W_final download");
+    return IPTTT_OK;
   }
-  s = run_layer(ctx, Hd, Xd, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, Od, Wfd, ws);
-  if (s != IPTTT_OK) return s;
-  if (T > 0 && (e = cudaMemcpyAsync(O_host, Od, act, cudaMemcpyDeviceToHost, ctx->stream)) != cudaSuccess)
-    return cuda_fail(ctx, e, "O download");
-  if ((e = cudaMemcpyAsync(W_final_host, Wfd, (size_t)B * d * d_ff * 4, cudaMemcpyDeviceToHost, ctx->stream)) !=
-      cudaSuccess)
-    return cuda_fail(ctx, e, "W_final download");
+  // fork the copy streams from the caller's stream, and start every sequence from W_down0
+  if ((e = cudaEventRecord(ctx->h_fork, ctx->stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(ctx->copy_in, ctx->h_fork, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(ctx->copy_out, ctx->h_fork, 0)) != cudaSuccess)
+    return cuda_fail(ctx, e, "copy fork");
+  if ((s = run_layer(ctx, nullptr, nullptr, W_gate, W_up, W_down0, W_target, conv_w, B, 0, d, d_ff, C, k, eta, dt,
+                     nullptr, Wst, ws)) != IPTTT_OK)
+    return s;
+  const size_t row_bytes = (size_t)T * d * es;  // one sequence in the host arrays
+  const int n_pieces = (int)((T + P - 1) / P);
+  for (int j = 0; j < n_pieces; ++j) {
+    const int64_t lo = j * P;
+    const int64_t len = (lo + P < T ? P : T - lo);
+    const size_t off = (size_t)B * lo * d * es;   // piece j's [B, len, d] block of the staging
+    const size_t width = (size_t)len * d * es;
+    cudaEvent_t in_done = ctx->piece_ev[2 * j], comp_done = ctx->piece_ev[2 * j + 1];
+    const uint8_t* hsrc = static_cast<const uint8_t*>(H_host) + (size_t)lo * d * es;
+    const uint8_t* xsrc = static_cast<const uint8_t*>(X0_host) + (size_t)lo * d * es;
+    if ((e = cudaMemcpy2DAsync(Hd + off, width, hsrc, row_bytes, width, (size_t)B, cudaMemcpyHostToDevice,
+                               ctx->copy_in)) != cudaSuccess ||
+        (e = cudaMemcpy2DAsync(Xd + off, width, xsrc, row_bytes, width, (size_t)B, cudaMemcpyHostToDevice,
+                               ctx->copy_in)) != cudaSuccess ||
+        (e = cudaEventRecord(in_done, ctx->copy_in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ctx->stream, in_done, 0)) != cudaSuccess)
+      return cuda_fail(ctx, e, "piece upload");
+    // continue every sequence from the state and conv halo the previous piece left
+    if ((s = run_layer(ctx, Hd + off, Xd + off, W_gate, W_up, nullptr, W_target, conv_w, B, len, d, d_ff, C, k, eta,
+                       dt, Od + off, Wst, ws, Wst, j > 0 ? halo[j & 1] : nullptr, halo[(j + 1) & 1])) != IPTTT_OK)
+      return s;
+    uint8_t* odst = static_cast<uint8_t*>(O_host) + (size_t)lo * d * es;
+    if ((e = cudaEventRecord(comp_done, ctx->stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ctx->copy_out, comp_done, 0)) != cudaSuccess ||
+        (e = cudaMemcpy2DAsync(odst, row_bytes, Od + off, width, width, (size_t)B, cudaMemcpyDeviceToHost,
+                               ctx->copy_out)) != cudaSuccess)
+      return cuda_fail(ctx, e, "piece download");
+  }
+  // the final state follows the last piece on copy_out; the caller's stream joins both copy streams
+  if ((e = cudaMemcpyAsync(W_final_host, Wst, state_bytes, cudaMemcpyDeviceToHost, ctx->copy_out)) != cudaSuccess ||
+      (e = cudaEventRecord(ctx->h_join, ctx->copy_out)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(ctx->stream, ctx->h_join, 0)) != cudaSuccess ||
+      (e = cudaEventRecord(ctx->h_join, ctx->copy_in)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(ctx->stream, ctx->h_join, 0)) != cudaSuccess)
+    return cuda_fail(ctx, e, "copy join");
   return IPTTT_OK;
 }
 
