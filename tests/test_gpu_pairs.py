@@ -67,7 +67,11 @@ def test_apply_pairs_match_single(ctx, B, T, d, f, C):
 
 
 @pytest.mark.parametrize("fused", [True, False])
-@pytest.mark.parametrize("B,T,d,f,C,k", [(2, 700, 256, 512, 256, 4), (1, 1100, 384, 768, 512, 3)])
+@pytest.mark.parametrize("B,T,d,f,C,k", [
+    (2, 700, 256, 512, 256, 4),
+    (1, 1100, 384, 768, 512, 3),
+    (3, 600, 1024, 4096, 256, 4),   # 192 pair units: more unit pairs than co-resident CTA pairs
+])
 def test_layer_pairs_match_single(ctx, fused, B, T, d, f, C, k):
     w, x = random_case(B, T, d, f, C, k, 2.0 / C, "bf16", 60 + T)
     xd = to_dev(x)
@@ -85,7 +89,7 @@ def test_layer_pairs_match_single(ctx, fused, B, T, d, f, C, k):
 
 @pytest.mark.parametrize("reverse_case", [False, True])
 @pytest.mark.parametrize("B,T,d,f,C", [(2, 300, 192, 384, 128), (1, 1024, 512, 1024, 256), (3, 130, 136, 264, 128),
-                                       (1, 5, 64, 64, 128)])
+                                       (1, 5, 64, 64, 128), (3, 600, 1024, 4096, 256)])
 def test_chunk_state_pairs_match_single(ctx, reverse_case, B, T, d, f, C):
     """The state kernel on pairs (256-row units) and on single CTAs (128-row units); the reverse
     scan is exercised through the backward pass."""
