@@ -470,6 +470,72 @@ def run_backward_bench(args, w):
     return 0
 
 
+def run_train_bench(args, w):
+    """Throughput of a training step of the layer on one GPU: ipttt_layer_forward_train (the
+    forward, keeping the activations the backward reads) then ipttt_layer_backward_saved (the
+    gradients of every input and weight from them), given dO and dW_final."""
+    import torch
+
+    import weight_mlp_layers_swiglu_b300 as pkg
+    from weight_mlp_layers_swiglu_b300.inputs import make_activations, make_weights
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    weights = {k: v.to(dev) for k, v in make_weights(w).items()}
+    acts = [make_activations(w, b) for b in range(w.B)]
+    H = torch.stack([a[0] for a in acts]).to(dev)
+    X0 = torch.stack([a[1] for a in acts]).to(dev)
+    g = torch.Generator(device="cpu").manual_seed(1234)
+    dO = torch.randn((w.B, w.T, w.d), generator=g).to(H.dtype).to(dev)
+    dWf = (torch.randn((w.B, w.d, w.d_ff), generator=g) * 0.01).to(dev)
+    ctx = pkg.Context(0)
+    code = pkg.dtype_code(H.dtype)
+    saved = torch.empty(pkg.saved_size(w.B, w.T, w.d, w.d_ff, w.C, w.k, code), dtype=torch.uint8, device=dev)
+    ws = torch.empty(pkg.backward_saved_workspace_size(w.B, w.T, w.d, w.d_ff, w.C, w.k, code), dtype=torch.uint8,
+                     device=dev)
+    O = torch.empty((w.B, w.T, w.d), dtype=H.dtype, device=dev)
+    Wf = torch.empty((w.B, w.d, w.d_ff), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ctx.layer_forward_train(H, X0, weights["W_gate"], weights["W_up"], weights["W_down0"], weights["W_target"],
+                                weights["conv_w"], w.C, w.eta, O=O, W_final=Wf, saved=saved)
+        ctx.layer_backward_saved(H, X0, weights["W_gate"], weights["W_up"], weights["W_target"], weights["conv_w"],
+                                 w.C, w.eta, saved, dO, dWf, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    if ctx.sync() != 0:
+        raise RuntimeError(f"device status during warm-up: {ctx.last_error()}")
+    with ClockSampler(0) as clocks:
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if ctx.sync() != 0:
+        raise RuntimeError(f"device status in the timed region: {ctx.last_error()}")
+    per_step = e0.elapsed_time(e1) / args.steps
+    peaks, peak_src = load_peaks()
+    flop = w.flops() + backward_flops(w)["algorithmic"]  # nothing is recomputed
+    tf = flop / (per_step * 1e-3) / 1e12
+    line = {"metric": "training-step tokens/s per In-Place-TTT MLP layer (forward + backward)",
+            "value": w.B * w.T / (per_step * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": workload_config(w) | {"pass": "forward_train + backward_saved (dO and dW_final given)"},
+            "tflops": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops_sustained"], "traffic": None,
+                         "peak_source": f"{peak_src} bf16 sustained", "flop_per_step": flop},
+            "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+    ctx.close()
+    return 0
+
+
 def e2e_leg(args, w, ctx, weights, H_host, X_host, dev, world):
     """The same metric end to end through the C ABI with host buffers: every step uploads H and
     X0 from pinned memory, runs the layer and downloads O and W_final."""
@@ -617,6 +683,8 @@ def main(argv=None):
                     help="run the bf16 GEMMs on single CTAs instead of CTA pairs (for comparison)")
     ap.add_argument("--unfused", action="store_true",
                     help="run steps (3)-(5) as the state kernel and the apply GEMM instead of one fused kernel")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step (forward keeping activations + backward from them) instead")
     ap.add_argument("--backward", action="store_true",
                     help="time the layer's backward pass instead (one GPU; its own JSON line)")
     args = ap.parse_args(argv)
@@ -633,6 +701,8 @@ def main(argv=None):
         return run_cp(args, w)
     if args.backward:
         return run_backward_bench(args, w)
+    if args.train:
+        return run_train_bench(args, w)
     if args.sweep:
         args.no_e2e, args.no_cpu_baseline, args.stream_tokens = True, True, 0
         if args.sweep == "chunk":

@@ -240,6 +240,47 @@ ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0,
                                   float* dW_down0, float* dW_target, float* dconv_w, void* workspace,
                                   size_t workspace_bytes);
 
+/* ---- training: the forward keeps what the backward pass reads ----
+ * ipttt_layer_forward_train computes what ipttt_layer_forward computes, bit for bit, and also
+ * keeps in `saved` the activations the backward pass would otherwise recompute: Z
+ * [B,T,d_ff], the gate and up pre-activations [A | U] [B,T,2 d_ff], Y = CausalConv1D(X0)
+ * [B,T,d], V = eta * Y W_target [B,T,d] and the weight of every chunk W_i [B,n,d,d_ff]
+ * (W_0 = W_down0 included), all dtype, then n*B+1 uint32 counters; each region 256-byte
+ * aligned.  ipttt_layer_backward_saved then runs only the backward half; it overwrites the
+ * [A | U] region with [dA | dU], so a saved buffer serves one backward call. */
+
+/* Bytes of the saved-activation buffer (host-only call).  Errors as ipttt_workspace_size. */
+ipttt_status ipttt_saved_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
+                              ipttt_dtype dtype, size_t* bytes);
+
+/* Bytes of device workspace ipttt_layer_backward_saved needs: dZ (fp32 only), dV, dY, the
+ * R_i stack, per-sequence dW_down0 and the conv-tap partial sums, as in
+ * ipttt_backward_workspace_size.  Errors as ipttt_workspace_size. */
+ipttt_status ipttt_backward_saved_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff,
+                                                 int64_t C, int k, ipttt_dtype dtype, size_t* bytes);
+
+/* The layer (arguments as ipttt_layer_forward) with `saved` (device, >= ipttt_saved_size()
+ * bytes, overwritten) in place of the workspace.  Errors as ipttt_layer_forward. */
+ipttt_status ipttt_layer_forward_train(ipttt_ctx* ctx, const void* H, const void* X0,
+                                       const void* W_gate, const void* W_up, const void* W_down0,
+                                       const void* W_target, const void* conv_w, int64_t B, int64_t T,
+                                       int64_t d, int64_t d_ff, int64_t C, int k, float eta,
+                                       ipttt_dtype dtype, void* O, float* W_final, void* saved,
+                                       size_t saved_bytes);
+
+/* The gradients of ipttt_layer_backward from a saved buffer that ipttt_layer_forward_train
+ * filled with the same inputs (W_down0 is not needed: every W_i is saved).  Arguments and
+ * outputs as ipttt_layer_backward; the workspace is >= ipttt_backward_saved_workspace_size()
+ * bytes.  The [A | U] region of `saved` is overwritten.  Errors as ipttt_layer_backward. */
+ipttt_status ipttt_layer_backward_saved(ipttt_ctx* ctx, const void* H, const void* X0,
+                                        const void* W_gate, const void* W_up, const void* W_target,
+                                        const void* conv_w, int64_t B, int64_t T, int64_t d,
+                                        int64_t d_ff, int64_t C, int k, float eta, ipttt_dtype dtype,
+                                        void* saved, size_t saved_bytes, const void* dO,
+                                        const float* dW_final, void* dH, void* dX0, float* dW_gate,
+                                        float* dW_up, float* dW_down0, float* dW_target,
+                                        float* dconv_w, void* workspace, size_t workspace_bytes);
+
 /* ---- the individual steps (the layer is exactly these calls in this order) ---- */
 
 /* Step (1), §3.1: Z[r] = SiLU(H[r] W_gate^T) * (H[r] W_up^T) for rows r < rows (rows = B*T).

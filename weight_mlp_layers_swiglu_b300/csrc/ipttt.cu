@@ -587,7 +587,7 @@ ipttt_status run_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff, int64_t
 // Returns false, having launched nothing, when the cooperative cluster launch is refused.
 bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
                               int64_t d, int64_t f, int64_t C, void* W_eff, float* W_final, void* O, uint32_t* ctr,
-                              const float* W_init, ipttt_status* st) {
+                              const float* W_init, bool write_first, ipttt_status* st) {
   const int64_t n = n_chunks_of(T, C);
   CUtensorMap mv, mz, mw_st, mf, mza, mw_ld, mw0, mo;
   *st = IPTTT_ERR_CUDA;
@@ -596,7 +596,7 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
       !map_3d(ctx, &mza, Z, B, T, f, 128) || !map_3d(ctx, &mw_ld, W_eff, B * n, d, f, 128) ||
       !map_3d(ctx, &mo, O, B, T, d, 32))
     return true;
-  if (W_init == nullptr) {
+  if (W_init == nullptr && !write_first) {
     if (!map_2d(ctx, &mw0, W0, d, f, 64, 128)) return true;
   } else {
     mw0 = mw_ld;  // unused: chunk 0 reads W_eff[b, 0]
@@ -612,7 +612,7 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
   p.s.n_units = ceil_div(f, state2::BNF);
   p.s.units = (int)(B * p.s.m_units * p.s.n_units);
   p.s.W0 = static_cast<const __nv_bfloat16*>(W0);
-  p.s.skip_first = W_init == nullptr ? 1 : 0;
+  p.s.skip_first = (W_init == nullptr && !write_first) ? 1 : 0;
   p.s.W_init = W_init;
   p.s.st = dev_status(ctx);
   p.a.m_tiles = (int)(C / gemm2::PAIR_M);
@@ -648,12 +648,14 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
   return true;
 }
 
+// write_first: W_eff[b, 0] is written (and chunk 0 applied from it) even without W_init.
 ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, int64_t B, int64_t T,
                                    int64_t d, int64_t f, int64_t C, void* W_eff, float* W_final, void* O,
-                                   uint32_t* ctr, const float* W_init = nullptr) {
+                                   uint32_t* ctr, const float* W_init = nullptr, bool write_first = false) {
   if (use_pairs(ctx) && ctx->fused_pairs && C % gemm2::PAIR_M == 0) {
     ipttt_status st;
-    if (launch_state_apply_pairs(ctx, V, Z, W0, B, T, d, f, C, W_eff, W_final, O, ctr, W_init, &st)) return st;
+    if (launch_state_apply_pairs(ctx, V, Z, W0, B, T, d, f, C, W_eff, W_final, O, ctr, W_init, write_first, &st))
+      return st;
   }
   const int64_t n = n_chunks_of(T, C);
   CUtensorMap mv, mz, mw_st, mf, mza, mw_ld, mw0, mo;
@@ -662,7 +664,7 @@ ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z,
       !map_3d(ctx, &mza, Z, B, T, f, 128) || !map_3d(ctx, &mw_ld, W_eff, B * n, d, f, 256) ||
       !map_3d(ctx, &mo, O, B, T, d, 32))
     return IPTTT_ERR_CUDA;
-  if (W_init == nullptr) {
+  if (W_init == nullptr && !write_first) {
     if (!map_2d(ctx, &mw0, W0, d, f, 64, 256)) return IPTTT_ERR_CUDA;
   } else {
     mw0 = mw_ld;  // unused: chunk 0 reads W_eff[b, 0]
@@ -678,7 +680,7 @@ ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z,
   p.s.n_units = ceil_div(f, state::BNF);
   p.s.units = (int)(B * p.s.m_units * p.s.n_units);
   p.s.W0 = static_cast<const __nv_bfloat16*>(W0);
-  p.s.skip_first = W_init == nullptr ? 1 : 0;
+  p.s.skip_first = (W_init == nullptr && !write_first) ? 1 : 0;
   p.s.W_init = W_init;
   p.s.st = dev_status(ctx);
   p.a.m_tiles = (int)(C / gemm::BM);
@@ -816,35 +818,123 @@ ipttt_status sgemm(ipttt_ctx* ctx, const float* A, int64_t a_sm, int64_t a_sk, c
   return check_launch(ctx, "sgemm launch");
 }
 
-struct BwdLayout {
-  size_t y, v, z, au, dz, dv, dy, wst, rst, dw0b, part, total;
-  int64_t strips;
+// Step (1) that also keeps the gate and up pre-activations AU = [A | U] ([rows, 2 d_ff]) for
+// the backward pass: bf16 through the SwiGLU GEMM's saving epilogue, fp32 as two GEMMs and an
+// elementwise combine.
+ipttt_status run_swiglu_save(ipttt_ctx* ctx, const void* H, const void* Wg, const void* Wu, int64_t BT, int64_t d,
+                             int64_t f, ipttt_dtype dt, void* Z, void* AU) {
+  ipttt_status s = IPTTT_OK;
+  if (BT == 0) return s;
+  if (dt == IPTTT_BF16) {
+    // [A | U] as [rows][2][d_ff]: a box never crosses from the gate half into the up half
+    CUtensorMap ma, mb0, mb1, mo, mx;
+    const uint64_t au_dims[3] = {(uint64_t)f, 2, (uint64_t)BT};
+    const uint64_t au_strides[2] = {(uint64_t)f * 2, (uint64_t)f * 4};
+    const uint32_t au_box[3] = {64, 1, 32};
+    if (!map_2d(ctx, &ma, H, BT, d, 64, 128) || !map_2d(ctx, &mb0, Wg, f, d, 64, 128) ||
+        !map_2d(ctx, &mb1, Wu, f, d, 64, 128) || !map_2d(ctx, &mo, Z, BT, f, 64, 32) ||
+        !encode_map(ctx, &mx, AU, 3, au_dims, au_strides, au_box))
+      return IPTTT_ERR_CUDA;
+    const bool pairs = use_pairs(ctx);
+    gemm::Params p{};
+    p.m_tiles = ceil_div(BT, pairs ? gemm2::PAIR_M : gemm::BM);
+    p.n_tiles = ceil_div(f, 128);
+    p.k_blocks = ceil_div(d, gemm::BK);
+    p.problems = 1;
+    p.group_m = pairs ? 8 : 16;
+    p.scale = 1.f;
+    p.st = dev_status(ctx);
+    const int tiles = p.m_tiles * p.n_tiles;
+    if (pairs) {
+      gemm2::tc_gemm2_kernel<gemm::kSwigluSave><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
+                                                 ctx->stream>>>(ma, mb0, mb1, mo, mx, p);
+    } else {
+      const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+      gemm::tc_gemm_kernel<gemm::kSwigluSave><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(
+          ma, mb0, mb1, mo, mx, p);
+    }
+    return check_launch(ctx, "swiglu save launch");
+  }
+  // A -> AU[:, :f], U -> AU[:, f:], then Z = SiLU(A) U
+  float* au = static_cast<float*>(AU);
+  if ((s = sgemm(ctx, static_cast<const float*>(H), d, 1, static_cast<const float*>(Wg), 1, d, au, 2 * f, BT, f, d,
+                 1.f, 0.f)) != IPTTT_OK ||
+      (s = sgemm(ctx, static_cast<const float*>(H), d, 1, static_cast<const float*>(Wu), 1, d, au + f, 2 * f, BT, f, d,
+                 1.f, 0.f)) != IPTTT_OK)
+    return s;
+  simt::swiglu_combine_kernel<float><<<ceil_div(BT * f, 256), 256, 0, ctx->stream>>>(au, static_cast<float*>(Z), BT,
+                                                                                     (int)f);
+  return check_launch(ctx, "combine launch");
+}
+
+// Forward activations the backward pass reads (all dtype): Z [B,T,d_ff], [A | U] [B,T,2 d_ff],
+// Y = conv(X0) [B,T,d], V = eta * Y W_target [B,T,d] and the W_i stack [B,n,d,d_ff] with every
+// slice (W_0 = W_down0 included); then the fused kernel's counters.  Each region 256-byte aligned.
+struct SavedLayout {
+  size_t z, au, y, v, wst, ctr, total;
 };
 
-BwdLayout bwd_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, int k, ipttt_dtype dt) {
+SavedLayout saved_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, ipttt_dtype dt) {
   const size_t es = esize(dt);
   const int64_t n = n_chunks_of(T, C);
-  BwdLayout L;
+  SavedLayout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
     off += align256(bytes);
     return at;
   };
-  L.y = take((size_t)B * T * d * es);
-  L.v = take((size_t)B * T * d * es);
   L.z = take((size_t)B * T * f * es);
   L.au = take((size_t)B * T * 2 * f * es);
+  L.y = take((size_t)B * T * d * es);
+  L.v = take((size_t)B * T * d * es);
+  L.wst = take((size_t)B * n * d * f * es);
+  L.ctr = take((size_t)(B * n + 1) * 4);
+  L.total = off;
+  return L;
+}
+
+struct SavedPtrs {
+  void *z, *au, *y, *v, *wst;
+  uint32_t* ctr;
+};
+
+SavedPtrs saved_ptrs(void* base, const SavedLayout& L) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  return SavedPtrs{b + L.z, b + L.au, b + L.y, b + L.v, b + L.wst, reinterpret_cast<uint32_t*>(b + L.ctr)};
+}
+
+// The backward pass's own scratch: dZ (fp32 path only), dV, dY, the R_i stack, per-sequence
+// dW_down0 (fp32) and the conv-tap partial sums (fp32).
+struct BwdScratch {
+  size_t dz, dv, dy, rst, dw0b, part, total;
+  int64_t strips;
+};
+
+BwdScratch scratch_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, int k, ipttt_dtype dt) {
+  const size_t es = esize(dt);
+  const int64_t n = n_chunks_of(T, C);
+  BwdScratch L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
   L.dz = take(dt == IPTTT_BF16 ? 0 : (size_t)B * T * f * es);  // bf16: dZ never leaves the GEMM epilogue
   L.dv = take((size_t)B * T * d * es);
   L.dy = take((size_t)B * T * d * es);
-  L.wst = take((size_t)B * n * d * f * es);
   L.rst = take((size_t)B * n * d * f * es);
   L.dw0b = take((size_t)B * d * f * 4);
   L.strips = B * ((T + simt::CONVW_STRIP - 1) / simt::CONVW_STRIP);
   L.part = take((size_t)L.strips * d * k * 4);
   L.total = off;
   return L;
+}
+
+// Workspace of the backward pass with recompute: the saved activations, then the scratch.
+size_t bwd_total(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, int k, ipttt_dtype dt) {
+  return saved_layout(B, T, d, f, C, dt).total + scratch_layout(B, T, d, f, C, k, dt).total;
 }
 
 // Pieces of a host-buffer call: a multiple of C near kPieceTokens, at most kMaxPieces of them.
@@ -882,22 +972,43 @@ HostLayout host_layout(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C, in
   return L;
 }
 
-// The backward pass (validated by the caller; T >= 1).
-ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
-                          const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d, int64_t f,
-                          int64_t C, int k, float eta, ipttt_dtype dt, const void* dO, const float* dW_final,
-                          void* dH, void* dX0, float* dWg, float* dWu, float* dW0, float* dWt, float* dcw, void* ws) {
+// Recompute of the forward activations the backward pass reads (Z, [A | U], Y, V and every W_i;
+// the forward's final state goes to W_fin_scratch).
+ipttt_status run_forward_saved(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
+                               const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d,
+                               int64_t f, int64_t C, int k, float eta, ipttt_dtype dt, const SavedPtrs& sv,
+                               float* W_fin_scratch) {
   ipttt_status s = IPTTT_OK;
-  const BwdLayout L = bwd_layout(B, T, d, f, C, k, dt);
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  void* Y = base + L.y;
-  void* V = base + L.v;
-  void* Z = base + L.z;
-  void* AU = base + L.au;
+  const int64_t BT = B * T;
+  if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  if ((s = run_swiglu_save(ctx, H, Wg, Wu, BT, d, f, dt, sv.z, sv.au)) != IPTTT_OK) return s;
+  if (Wt != nullptr) {
+    if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, sv.y)) != IPTTT_OK) return s;
+    if ((s = run_target_gemm(ctx, sv.y, Wt, BT, d, eta, dt, sv.v)) != IPTTT_OK) return s;
+  } else if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, sv.v, nullptr, eta)) != IPTTT_OK) {  // V = eta * conv(X0)
+    return s;
+  }
+  return run_state(ctx, sv.v, sv.z, W0, B, T, d, f, C, dt, sv.wst, W_fin_scratch, false);
+}
+
+// The backward pass from the saved forward activations (validated by the caller; T >= 1).  It
+// overwrites sv.au with [dA | dU].
+ipttt_status run_backward_core(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
+                               const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d, int64_t f, int64_t C,
+                               int k, float eta, ipttt_dtype dt, const void* dO, const float* dW_final, void* dH,
+                               void* dX0, float* dWg, float* dWu, float* dW0, float* dWt, float* dcw,
+                               const SavedPtrs& sv, void* scratch) {
+  ipttt_status s = IPTTT_OK;
+  const BwdScratch L = scratch_layout(B, T, d, f, C, k, dt);
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  const void* Y = sv.y;
+  const void* V = sv.v;
+  const void* Z = sv.z;
+  void* AU = sv.au;
+  const void* Wst = sv.wst;
   void* dZ = base + L.dz;
   void* dV = base + L.dv;
   void* dY = base + L.dy;
-  void* Wst = base + L.wst;
   void* Rst = base + L.rst;
   float* dW0b = reinterpret_cast<float*>(base + L.dw0b);
   float* part = reinterpret_cast<float*>(base + L.part);
@@ -906,59 +1017,7 @@ ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const v
   const int64_t CT = (BT + 255) / 256 * 256;  // all tokens as one chunk (flat GEMMs and reductions)
   const bool bf16 = dt == IPTTT_BF16;
   const int64_t df = d * f;
-  if (bf16) {
-    if ((s = ensure_attrs(ctx)) != IPTTT_OK) return s;
-    // forward recompute: Z and the pre-activations [A | U]
-    {
-      // [A | U] as [rows][2][d_ff]: a box never crosses from the gate half into the up half
-      CUtensorMap ma, mb0, mb1, mo, mx;
-      const uint64_t au_dims[3] = {(uint64_t)f, 2, (uint64_t)BT};
-      const uint64_t au_strides[2] = {(uint64_t)f * 2, (uint64_t)f * 4};
-      const uint32_t au_box[3] = {64, 1, 32};
-      if (!map_2d(ctx, &ma, H, BT, d, 64, 128) || !map_2d(ctx, &mb0, Wg, f, d, 64, 128) ||
-          !map_2d(ctx, &mb1, Wu, f, d, 64, 128) || !map_2d(ctx, &mo, Z, BT, f, 64, 32) ||
-          !encode_map(ctx, &mx, AU, 3, au_dims, au_strides, au_box))
-        return IPTTT_ERR_CUDA;
-      const bool pairs = use_pairs(ctx);
-      gemm::Params p{};
-      p.m_tiles = ceil_div(BT, pairs ? gemm2::PAIR_M : gemm::BM);
-      p.n_tiles = ceil_div(f, 128);
-      p.k_blocks = ceil_div(d, gemm::BK);
-      p.problems = 1;
-      p.group_m = pairs ? 8 : 16;
-      p.scale = 1.f;
-      p.st = dev_status(ctx);
-      const int tiles = p.m_tiles * p.n_tiles;
-      if (pairs) {
-        gemm2::tc_gemm2_kernel<gemm::kSwigluSave><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
-                                                   ctx->stream>>>(ma, mb0, mb1, mo, mx, p);
-      } else {
-        const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
-        gemm::tc_gemm_kernel<gemm::kSwigluSave><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, ctx->stream>>>(
-            ma, mb0, mb1, mo, mx, p);
-      }
-      if ((s = check_launch(ctx, "swiglu save launch")) != IPTTT_OK) return s;
-    }
-  } else {
-    // A -> AU[:, :f], U -> AU[:, f:], then Z = SiLU(A) U
-    float* au = static_cast<float*>(AU);
-    if ((s = sgemm(ctx, static_cast<const float*>(H), d, 1, static_cast<const float*>(Wg), 1, d, au, 2 * f, BT, f, d,
-                   1.f, 0.f)) != IPTTT_OK ||
-        (s = sgemm(ctx, static_cast<const float*>(H), d, 1, static_cast<const float*>(Wu), 1, d, au + f, 2 * f, BT, f,
-                   d, 1.f, 0.f)) != IPTTT_OK)
-      return s;
-    simt::swiglu_combine_kernel<float><<<ceil_div(BT * f, 256), 256, 0, ctx->stream>>>(au, static_cast<float*>(Z),
-                                                                                       BT, (int)f);
-    if ((s = check_launch(ctx, "combine launch")) != IPTTT_OK) return s;
-  }
-  // target and forward weights of every chunk (the forward's W_final goes to scratch)
-  if (Wt != nullptr) {
-    if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, Y)) != IPTTT_OK) return s;
-    if ((s = run_target_gemm(ctx, Y, Wt, BT, d, eta, dt, V)) != IPTTT_OK) return s;
-  } else if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, V, nullptr, eta)) != IPTTT_OK) {  // V = eta * conv(X0)
-    return s;
-  }
-  if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, dW0b, false)) != IPTTT_OK) return s;
+  if (bf16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
   if (bf16) {
     // reverse scan: R_i = dW_final + sum_{l>i} dO_l^T Z_l, final = dW_final + sum_i dO_i^T Z_i
     if ((s = launch_state_general(ctx, dO, d, Z, f, B, T, d, f, C, nullptr, dW_final, false, true, Rst,
@@ -1057,6 +1116,21 @@ ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const v
   return check_launch(ctx, "batch sum launch");
 }
 
+// The backward pass with the forward recomputed into the first part of the workspace.
+ipttt_status run_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
+                          const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d, int64_t f,
+                          int64_t C, int k, float eta, ipttt_dtype dt, const void* dO, const float* dW_final,
+                          void* dH, void* dX0, float* dWg, float* dWu, float* dW0, float* dWt, float* dcw, void* ws) {
+  const SavedLayout SL = saved_layout(B, T, d, f, C, dt);
+  const SavedPtrs sv = saved_ptrs(ws, SL);
+  void* scratch = static_cast<uint8_t*>(ws) + SL.total;
+  float* w_fin = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + scratch_layout(B, T, d, f, C, k, dt).dw0b);
+  ipttt_status s = run_forward_saved(ctx, H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, C, k, eta, dt, sv, w_fin);
+  if (s != IPTTT_OK) return s;
+  return run_backward_core(ctx, H, X0, Wg, Wu, Wt, cw, B, T, d, f, C, k, eta, dt, dO, dW_final, dH, dX0, dWg, dWu,
+                           dW0, dWt, dcw, sv, scratch);
+}
+
 void mark(ipttt_ctx* ctx, int call, int which, cudaStream_t stream) {
   if (call >= 0) cudaEventRecord(ctx->events[(size_t)call * kEventsPerCall + which], stream);
 }
@@ -1064,10 +1138,13 @@ void mark(ipttt_ctx* ctx, int call, int which, cudaStream_t stream) {
 // The layer on device buffers, validated by the caller.
 // W_init (optional, fp32 [B, d, f]): per-sequence starting state instead of W0; halo_in /
 // halo_out (optional, [B, k-1, d]): the X0 rows before this call / after it (resumed calls).
+// sv (optional, with ws unused then): the training forward, which keeps the activations the
+// backward pass reads (Z, [A | U], Y, V and every W_i, W_0 included) in the saved buffer.
 ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
                        const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d, int64_t f,
                        int64_t C, int k, float eta, ipttt_dtype dt, void* O, float* W_final, void* ws,
-                       const float* W_init = nullptr, const void* halo_in = nullptr, void* halo_out = nullptr) {
+                       const float* W_init = nullptr, const void* halo_in = nullptr, void* halo_out = nullptr,
+                       const SavedPtrs* sv = nullptr) {
   if (B == 0) return IPTTT_OK;
   if (halo_out != nullptr && k > 1) {
     const int64_t nh = B * (k - 1) * d;
@@ -1103,10 +1180,10 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
   const WsLayout L = ws_layout(B, T, d, f, C, dt);
   uint8_t* base = static_cast<uint8_t*>(ws);
-  void* Y = base + L.y;
-  void* V = base + L.v;
-  void* Z = base + L.z;
-  void* Wst = base + L.w;
+  void* Y = sv ? sv->y : base + L.y;
+  void* V = sv ? sv->v : base + L.v;
+  void* Z = sv ? sv->z : base + L.z;
+  void* Wst = sv ? sv->wst : base + L.w;
   int call = -1;
   if (ctx->timing && ctx->timed_calls < kMaxTimedCalls) {
     call = ctx->timed_calls++;
@@ -1130,13 +1207,15 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
     if (s != IPTTT_OK) return s;
   }
   if ((e = cudaEventRecord(ctx->join, ctx->side)) != cudaSuccess) return cuda_fail(ctx, e, "join record");
-  if ((s = run_swiglu(ctx, H, Wg, Wu, B * T, d, f, dt, Z)) != IPTTT_OK) return s;
+  if ((s = sv ? run_swiglu_save(ctx, H, Wg, Wu, B * T, d, f, dt, Z, sv->au)
+              : run_swiglu(ctx, H, Wg, Wu, B * T, d, f, dt, Z)) != IPTTT_OK)
+    return s;
   mark(ctx, call, kEvSwigluEnd, ctx->stream);
   if ((e = cudaStreamWaitEvent(ctx->stream, ctx->join, 0)) != cudaSuccess) return cuda_fail(ctx, e, "join");
   mark(ctx, call, kEvJoined, ctx->stream);
   const bool bf16 = dt == IPTTT_BF16;  // W_eff[b, 0] = W_down0: the apply reads W_down0 itself
   const bool fuse = bf16 && ctx->fused_tail && ctx->coop;
-  uint32_t* ctr = reinterpret_cast<uint32_t*>(base + L.ctr);
+  uint32_t* ctr = sv ? sv->ctr : reinterpret_cast<uint32_t*>(base + L.ctr);
   const int n_ctr = (int)(B * n_chunks_of(T, C) + 1);
   if (Wt != nullptr) {
     if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V, fuse ? ctr : nullptr, fuse ? n_ctr : 0)) != IPTTT_OK)
@@ -1147,15 +1226,17 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   }
   mark(ctx, call, kEvTargetEnd, ctx->stream);
   if (fuse) {
-    if ((s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr, W_init)) != IPTTT_OK)
+    if ((s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr, W_init, sv != nullptr)) !=
+        IPTTT_OK)
       return s;
     mark(ctx, call, kEvStateEnd, ctx->stream);
     mark(ctx, call, kEvApplyEnd, ctx->stream);
     if (call >= 0) ctx->timed_fused[call] = 1;
   } else {
-    if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, bf16, W_init)) != IPTTT_OK) return s;
+    const bool skip_first = bf16 && sv == nullptr;  // the training forward keeps W_0 in the stack too
+    if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, skip_first, W_init)) != IPTTT_OK) return s;
     mark(ctx, call, kEvStateEnd, ctx->stream);
-    const void* w0_first = (bf16 && W_init == nullptr) ? W0 : nullptr;
+    const void* w0_first = (skip_first && W_init == nullptr) ? W0 : nullptr;
     if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, w0_first)) != IPTTT_OK) return s;
     mark(ctx, call, kEvApplyEnd, ctx->stream);
   }
@@ -1165,10 +1246,12 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
 }
 
 // Validation of the device-buffer layer call (everything except the buffers' residency).
+// ws_need: bytes the workspace must hold (0: the layer's own, ipttt_workspace_size()).
 ipttt_status validate_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
                             const void* W0, const void* Wt, const void* cw, int64_t B, int64_t T, int64_t d,
                             int64_t f, int64_t C, int k, float eta, ipttt_dtype dt, const void* O,
-                            const float* W_final, const void* ws, size_t ws_bytes, bool check_overlap) {
+                            const float* W_final, const void* ws, size_t ws_bytes, bool check_overlap,
+                            size_t ws_need = 0) {
   ipttt_status s = check_shape(ctx, B, T, d, f, C, k, dt);
   if (s != IPTTT_OK) return s;
   if (!std::isfinite(eta)) {
@@ -1200,9 +1283,9 @@ ipttt_status validate_layer(ipttt_ctx* ctx, const void* H, const void* X0, const
     set_err(ctx, "W_target is not 16-byte aligned");
     return IPTTT_ERR_INVALID_ARG;
   }
-  const WsLayout L = ws_layout(B, T, d, f, C, dt);
-  if (T > 0 && ws_bytes < L.total) {
-    set_err(ctx, "workspace too small: %zu < %zu bytes", ws_bytes, L.total);
+  const size_t need = ws_need != 0 ? ws_need : ws_layout(B, T, d, f, C, dt).total;
+  if (T > 0 && ws_bytes < need) {
+    set_err(ctx, "workspace too small: %zu < %zu bytes", ws_bytes, need);
     return IPTTT_ERR_WORKSPACE;
   }
   if (check_overlap) {
@@ -1216,7 +1299,7 @@ ipttt_status validate_layer(ipttt_ctx* ctx, const void* H, const void* X0, const
                                {cw, (size_t)d * k * es, "conv_w"},
                                {O, act, "O"},
                                {W_final, (size_t)B * d * f * 4, "W_final"},
-                               {ws, T > 0 ? L.total : 0, "workspace"}};
+                               {ws, T > 0 ? need : 0, "workspace"}};
     std::vector<Region> outs = {all[7], all[8], all[9]};
     std::string what;
     if (find_overlap(outs, all, what)) {
@@ -1432,17 +1515,21 @@ ipttt_status ipttt_backward_workspace_size(int64_t B, int64_t T, int64_t d, int6
   if (!bytes) return IPTTT_ERR_INVALID_ARG;
   const ipttt_status s = check_shape(nullptr, B, T, d, d_ff, C, k, dt);
   if (s != IPTTT_OK) return s;
-  *bytes = bwd_layout(B, T, d, d_ff, C, k, dt).total;
+  *bytes = bwd_total(B, T, d, d_ff, C, k, dt);
   return IPTTT_OK;
 }
 
-ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
-                                  const void* W_up, const void* W_down0, const void* W_target, const void* conv_w,
-                                  int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k, float eta,
-                                  ipttt_dtype dt, const void* dO, const float* dW_final, void* dH, void* dX0,
-                                  float* dW_gate, float* dW_up, float* dW_down0, float* dW_target, float* dconv_w,
-                                  void* ws, size_t ws_bytes) {
-  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+namespace {
+
+// Argument checks shared by the two backward entries.  W_down0 is read only by the recomputing
+// entry (need_w0); `saved` (the second entry's saved activations, NULL for the first) is an
+// input that the call overwrites.
+ipttt_status check_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate, const void* W_up,
+                            const void* W_down0, bool need_w0, const void* W_target, const void* conv_w, int64_t B,
+                            int64_t T, int64_t d, int64_t d_ff, int64_t C, int k, float eta, ipttt_dtype dt,
+                            const void* dO, const float* dW_final, void* dH, void* dX0, float* dW_gate, float* dW_up,
+                            float* dW_down0, float* dW_target, float* dconv_w, const void* saved, size_t saved_need,
+                            size_t saved_bytes, void* ws, size_t ws_need, size_t ws_bytes) {
   ipttt_status s = check_shape(ctx, B, T, d, d_ff, C, k, dt);
   if (s != IPTTT_OK) return s;
   if (!std::isfinite(eta)) {
@@ -1458,15 +1545,17 @@ ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0,
     return IPTTT_ERR_UNSUPPORTED;
   }
   const bool work = B > 0 && T > 0;
+  const bool with_saved = saved_need > 0;
   struct P {
     const void* p;
     const char* n;
     bool needed;
   } ptrs[] = {{H, "H", work},         {X0, "X0", work},         {W_gate, "W_gate", work}, {W_up, "W_up", work},
-              {W_down0, "W_down0", work}, {conv_w, "conv_w", work}, {dO, "dO", work},       {dH, "dH", work},
+              {W_down0, "W_down0", work && need_w0}, {conv_w, "conv_w", work}, {dO, "dO", work}, {dH, "dH", work},
               {dX0, "dX0", work},     {dW_gate, "dW_gate", true}, {dW_up, "dW_up", true}, {dW_down0, "dW_down0", true},
               {dconv_w, "dconv_w", true}, {ws, "workspace", work}, {W_target, "W_target", false},
-              {dW_target, "dW_target", W_target != nullptr}, {dW_final, "dW_final", false}};
+              {dW_target, "dW_target", W_target != nullptr}, {dW_final, "dW_final", false},
+              {saved, "saved", work && with_saved}};
   for (const P& q : ptrs) {
     if (q.needed && !q.p) {
       set_err(ctx, "%s is NULL", q.n);
@@ -1477,9 +1566,12 @@ ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0,
       return IPTTT_ERR_INVALID_ARG;
     }
   }
-  const BwdLayout L = bwd_layout(B, T, d, d_ff, C, k, dt);
-  if (work && ws_bytes < L.total) {
-    set_err(ctx, "workspace too small: %zu < %zu bytes", ws_bytes, L.total);
+  if (work && ws_bytes < ws_need) {
+    set_err(ctx, "workspace too small: %zu < %zu bytes", ws_bytes, ws_need);
+    return IPTTT_ERR_WORKSPACE;
+  }
+  if (work && with_saved && saved_bytes < saved_need) {
+    set_err(ctx, "saved-activation buffer too small: %zu < %zu bytes", saved_bytes, saved_need);
     return IPTTT_ERR_WORKSPACE;
   }
   const size_t es = esize(dt);
@@ -1488,7 +1580,7 @@ ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0,
                              {X0, act, "X0"},
                              {W_gate, wdf, "W_gate"},
                              {W_up, wdf, "W_up"},
-                             {W_down0, wdf, "W_down0"},
+                             {W_down0, need_w0 ? wdf : 0, "W_down0"},
                              {W_target, (size_t)d * d * es, "W_target"},
                              {conv_w, (size_t)d * k * es, "conv_w"},
                              {dO, act, "dO"},
@@ -1500,30 +1592,108 @@ ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0,
                              {dW_down0, gdf, "dW_down0"},
                              {dW_target, W_target ? (size_t)d * d * 4 : 0, "dW_target"},
                              {dconv_w, (size_t)d * k * 4, "dconv_w"},
-                             {ws, work ? L.total : 0, "workspace"}};
+                             {ws, work ? ws_need : 0, "workspace"},
+                             {saved, work && with_saved ? saved_need : 0, "saved"}};
   std::vector<Region> outs(all.begin() + 9, all.end());
   std::string what;
   if (find_overlap(outs, all, what)) {
     set_err(ctx, "overlapping buffers: %s", what.c_str());
     return IPTTT_ERR_INVALID_ARG;
   }
+  return IPTTT_OK;
+}
+
+// No tokens: every gradient is zero except dW_down0 = sum_b dW_final[b].
+ipttt_status backward_no_tokens(ipttt_ctx* ctx, int64_t B, int64_t d, int64_t d_ff, int k, const float* dW_final,
+                                float* dW_gate, float* dW_up, float* dW_down0, float* dW_target, float* dconv_w) {
+  const size_t gdf = (size_t)d * d_ff * 4;
+  cudaMemsetAsync(dW_gate, 0, gdf, ctx->stream);
+  cudaMemsetAsync(dW_up, 0, gdf, ctx->stream);
+  if (dW_target) cudaMemsetAsync(dW_target, 0, (size_t)d * d * 4, ctx->stream);
+  cudaMemsetAsync(dconv_w, 0, (size_t)d * k * 4, ctx->stream);
+  if (dW_final != nullptr && B > 0)
+    simt::sum_strips_kernel<<<ceil_div(d * d_ff, 256), 256, 0, ctx->stream>>>(dW_final, dW_down0, (int)B, d * d_ff);
+  else
+    cudaMemsetAsync(dW_down0, 0, gdf, ctx->stream);
+  return check_launch(ctx, "empty backward");
+}
+
+}  // namespace
+
+ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                  const void* W_up, const void* W_down0, const void* W_target, const void* conv_w,
+                                  int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k, float eta,
+                                  ipttt_dtype dt, const void* dO, const float* dW_final, void* dH, void* dX0,
+                                  float* dW_gate, float* dW_up, float* dW_down0, float* dW_target, float* dconv_w,
+                                  void* ws, size_t ws_bytes) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  const ipttt_status s = check_backward(ctx, H, X0, W_gate, W_up, W_down0, true, W_target, conv_w, B, T, d, d_ff, C,
+                                        k, eta, dt, dO, dW_final, dH, dX0, dW_gate, dW_up, dW_down0, dW_target,
+                                        dconv_w, nullptr, 0, 0, ws, bwd_total(B, T, d, d_ff, C, k, dt), ws_bytes);
+  if (s != IPTTT_OK) return s;
   DeviceGuard g(ctx->device);
-  if (!work) {
-    // no tokens: every gradient is zero except dW_down0 = sum_b dW_final[b]
-    cudaMemsetAsync(dW_gate, 0, gdf, ctx->stream);
-    cudaMemsetAsync(dW_up, 0, gdf, ctx->stream);
-    if (dW_target) cudaMemsetAsync(dW_target, 0, (size_t)d * d * 4, ctx->stream);
-    cudaMemsetAsync(dconv_w, 0, (size_t)d * k * 4, ctx->stream);
-    if (dW_final != nullptr && B > 0) {
-      simt::sum_strips_kernel<<<ceil_div(d * d_ff, 256), 256, 0, ctx->stream>>>(dW_final, dW_down0, (int)B,
-                                                                                 d * d_ff);
-    } else {
-      cudaMemsetAsync(dW_down0, 0, gdf, ctx->stream);
-    }
-    return check_launch(ctx, "empty backward");
-  }
+  if (B == 0 || T == 0)
+    return backward_no_tokens(ctx, B, d, d_ff, k, dW_final, dW_gate, dW_up, dW_down0, dW_target, dconv_w);
   return run_backward(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, dO, dW_final,
                       dH, dX0, dW_gate, dW_up, dW_down0, dW_target, dconv_w, ws);
+}
+
+ipttt_status ipttt_saved_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k, ipttt_dtype dt,
+                              size_t* bytes) {
+  if (!bytes) return IPTTT_ERR_INVALID_ARG;
+  const ipttt_status s = check_shape(nullptr, B, T, d, d_ff, C, k, dt);
+  if (s != IPTTT_OK) return s;
+  *bytes = saved_layout(B, T, d, d_ff, C, dt).total;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_backward_saved_workspace_size(int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C, int k,
+                                                 ipttt_dtype dt, size_t* bytes) {
+  if (!bytes) return IPTTT_ERR_INVALID_ARG;
+  const ipttt_status s = check_shape(nullptr, B, T, d, d_ff, C, k, dt);
+  if (s != IPTTT_OK) return s;
+  *bytes = scratch_layout(B, T, d, d_ff, C, k, dt).total;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_layer_forward_train(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                       const void* W_up, const void* W_down0, const void* W_target,
+                                       const void* conv_w, int64_t B, int64_t T, int64_t d, int64_t d_ff, int64_t C,
+                                       int k, float eta, ipttt_dtype dt, void* O, float* W_final, void* saved,
+                                       size_t saved_bytes) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  const size_t need = saved_layout(B, T, d, d_ff, C, dt).total;
+  ipttt_status s = validate_layer(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt,
+                                  O, W_final, saved, saved_bytes, true, need);
+  if (s != IPTTT_OK) return s;
+  DeviceGuard g(ctx->device);
+  if (B == 0 || T == 0)
+    return run_layer(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, O, W_final,
+                     saved);
+  const SavedPtrs sv = saved_ptrs(saved, saved_layout(B, T, d, d_ff, C, dt));
+  return run_layer(ctx, H, X0, W_gate, W_up, W_down0, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, O, W_final,
+                   nullptr, nullptr, nullptr, nullptr, &sv);
+}
+
+ipttt_status ipttt_layer_backward_saved(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                        const void* W_up, const void* W_target, const void* conv_w, int64_t B,
+                                        int64_t T, int64_t d, int64_t d_ff, int64_t C, int k, float eta,
+                                        ipttt_dtype dt, void* saved, size_t saved_bytes, const void* dO,
+                                        const float* dW_final, void* dH, void* dX0, float* dW_gate, float* dW_up,
+                                        float* dW_down0, float* dW_target, float* dconv_w, void* ws,
+                                        size_t ws_bytes) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  const SavedLayout SL = saved_layout(B, T, d, d_ff, C, dt);
+  const ipttt_status s =
+      check_backward(ctx, H, X0, W_gate, W_up, nullptr, false, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, dO,
+                     dW_final, dH, dX0, dW_gate, dW_up, dW_down0, dW_target, dconv_w, saved, SL.total, saved_bytes, ws,
+                     scratch_layout(B, T, d, d_ff, C, k, dt).total, ws_bytes);
+  if (s != IPTTT_OK) return s;
+  DeviceGuard g(ctx->device);
+  if (B == 0 || T == 0)
+    return backward_no_tokens(ctx, B, d, d_ff, k, dW_final, dW_gate, dW_up, dW_down0, dW_target, dconv_w);
+  return run_backward_core(ctx, H, X0, W_gate, W_up, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt, dO, dW_final, dH,
+                           dX0, dW_gate, dW_up, dW_down0, dW_target, dconv_w, saved_ptrs(saved, SL), ws);
 }
 
 ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,

@@ -52,6 +52,14 @@ _SIGNATURES = {
                                       [c_i64] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "ipttt_layer_backward": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int]
                              + [c_vp] * 10 + [ctypes.c_size_t]),
+    "ipttt_saved_size": (ctypes.c_int, [c_i64] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "ipttt_backward_saved_workspace_size": (ctypes.c_int, [c_i64] * 5 + [ctypes.c_int, ctypes.c_int,
+                                                                         ctypes.POINTER(ctypes.c_size_t)]),
+    "ipttt_layer_forward_train": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int]
+                                  + [c_vp] * 3 + [ctypes.c_size_t]),
+    "ipttt_layer_backward_saved": (ctypes.c_int, [c_vp] * 7 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                                                             c_vp, ctypes.c_size_t] + [c_vp] * 10
+                                   + [ctypes.c_size_t]),
     "ipttt_swiglu": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, c_vp]),
     "ipttt_target": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_int, c_vp, c_vp]),
     "ipttt_chunk_state": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 5 + [ctypes.c_int, c_vp, c_vp]),
@@ -114,11 +122,23 @@ def workspace_size(B, T, d, d_ff, C, k, dtype: int, host: bool = False) -> int:
 
 
 def backward_workspace_size(B, T, d, d_ff, C, k, dtype: int) -> int:
+    return _size_query("ipttt_backward_workspace_size", B, T, d, d_ff, C, k, dtype)
+
+
+def _size_query(fn: str, B, T, d, d_ff, C, k, dtype: int) -> int:
     out = ctypes.c_size_t(0)
-    st = load().ipttt_backward_workspace_size(B, T, d, d_ff, C, k, dtype, ctypes.byref(out))
+    st = getattr(load(), fn)(B, T, d, d_ff, C, k, dtype, ctypes.byref(out))
     if st != IPTTT_OK:
-        raise IptttError(st, f"backward_workspace_size(B={B}, T={T}, d={d}, d_ff={d_ff}, C={C}, k={k})")
+        raise IptttError(st, f"{fn}(B={B}, T={T}, d={d}, d_ff={d_ff}, C={C}, k={k})")
     return out.value
+
+
+def saved_size(B, T, d, d_ff, C, k, dtype: int) -> int:
+    return _size_query("ipttt_saved_size", B, T, d, d_ff, C, k, dtype)
+
+
+def backward_saved_workspace_size(B, T, d, d_ff, C, k, dtype: int) -> int:
+    return _size_query("ipttt_backward_saved_workspace_size", B, T, d, d_ff, C, k, dtype)
 
 
 def layer_launches(B, T, dtype: int) -> int:
@@ -253,12 +273,7 @@ class Context:
         if dW_final is not None:
             _need(dW_final, "dW_final", (B, d, f), torch.float32, dev)
         code = dtype_code(dt)
-        f32 = dict(dtype=torch.float32, device=dev)
-        g = {"H": torch.empty((B, T, d), dtype=dt, device=dev), "X0": torch.empty((B, T, d), dtype=dt, device=dev),
-             "W_gate": torch.empty((f, d), **f32), "W_up": torch.empty((f, d), **f32),
-             "W_down0": torch.empty((d, f), **f32),
-             "W_target": torch.empty((d, d), **f32) if W_target is not None else None,
-             "conv_w": torch.empty((d, k), **f32)}
+        g = self._grad_buffers(B, T, d, f, k, dt, W_target is not None)
         if workspace is None:
             n = backward_workspace_size(B, T, d, f, C, k, code)
             workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
@@ -269,6 +284,68 @@ class Context:
             _ptr(workspace), workspace.numel() * workspace.element_size())
         self._check(st, "layer_backward")
         return g
+
+    def layer_forward_train(self, H, X0, W_gate, W_up, W_down0, W_target, conv_w, C: int, eta: float, O=None,
+                            W_final=None, saved=None):
+        """layer_forward that also fills a saved-activation buffer for layer_backward_saved.
+        Returns (O, W_final, saved)."""
+        B, T, d = H.shape
+        f = W_gate.shape[0]
+        k = conv_w.shape[1]
+        dt, dev = H.dtype, self.device
+        for t, n, s in ((H, "H", (B, T, d)), (X0, "X0", (B, T, d)), (W_gate, "W_gate", (f, d)),
+                        (W_up, "W_up", (f, d)), (W_down0, "W_down0", (d, f)), (conv_w, "conv_w", (d, k))):
+            _need(t, n, s, dt, dev)
+        if W_target is not None:
+            _need(W_target, "W_target", (d, d), dt, dev)
+        code = dtype_code(dt)
+        O = O if O is not None else torch.empty((B, T, d), dtype=dt, device=dev)
+        W_final = W_final if W_final is not None else torch.empty((B, d, f), dtype=torch.float32, device=dev)
+        if saved is None:
+            saved = torch.empty(max(saved_size(B, T, d, f, C, k, code), 256), dtype=torch.uint8, device=dev)
+        st = self.lib.ipttt_layer_forward_train(self.h, _ptr(H), _ptr(X0), _ptr(W_gate), _ptr(W_up), _ptr(W_down0),
+                                                _ptr(W_target), _ptr(conv_w), B, T, d, f, C, k, float(eta), code,
+                                                _ptr(O), _ptr(W_final), _ptr(saved),
+                                                saved.numel() * saved.element_size())
+        self._check(st, "layer_forward_train")
+        return O, W_final, saved
+
+    def layer_backward_saved(self, H, X0, W_gate, W_up, W_target, conv_w, C: int, eta: float, saved, dO,
+                             dW_final=None, workspace=None):
+        """Gradients from a buffer filled by layer_forward_train (which this call overwrites in part).
+        Returns the dict of layer_backward."""
+        B, T, d = H.shape
+        f = W_gate.shape[0]
+        k = conv_w.shape[1]
+        dt, dev = H.dtype, self.device
+        for t, n, s in ((H, "H", (B, T, d)), (X0, "X0", (B, T, d)), (W_gate, "W_gate", (f, d)),
+                        (W_up, "W_up", (f, d)), (conv_w, "conv_w", (d, k)), (dO, "dO", (B, T, d))):
+            _need(t, n, s, dt, dev)
+        if W_target is not None:
+            _need(W_target, "W_target", (d, d), dt, dev)
+        if dW_final is not None:
+            _need(dW_final, "dW_final", (B, d, f), torch.float32, dev)
+        code = dtype_code(dt)
+        g = self._grad_buffers(B, T, d, f, k, dt, W_target is not None)
+        if workspace is None:
+            n = backward_saved_workspace_size(B, T, d, f, C, k, code)
+            workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+        st = self.lib.ipttt_layer_backward_saved(
+            self.h, _ptr(H), _ptr(X0), _ptr(W_gate), _ptr(W_up), _ptr(W_target), _ptr(conv_w), B, T, d, f, C, k,
+            float(eta), code, _ptr(saved), saved.numel() * saved.element_size(), _ptr(dO), _ptr(dW_final),
+            _ptr(g["H"]), _ptr(g["X0"]), _ptr(g["W_gate"]), _ptr(g["W_up"]), _ptr(g["W_down0"]), _ptr(g["W_target"]),
+            _ptr(g["conv_w"]), _ptr(workspace), workspace.numel() * workspace.element_size())
+        self._check(st, "layer_backward_saved")
+        return g
+
+    def _grad_buffers(self, B, T, d, f, k, dt, with_target: bool) -> dict:
+        dev = self.device
+        f32 = dict(dtype=torch.float32, device=dev)
+        return {"H": torch.empty((B, T, d), dtype=dt, device=dev), "X0": torch.empty((B, T, d), dtype=dt, device=dev),
+                "W_gate": torch.empty((f, d), **f32), "W_up": torch.empty((f, d), **f32),
+                "W_down0": torch.empty((d, f), **f32),
+                "W_target": torch.empty((d, d), **f32) if with_target else None,
+                "conv_w": torch.empty((d, k), **f32)}
 
     def layer_resume(self, H, X0, W_gate, W_up, W_target, conv_w, W_state, X0_halo, C: int, eta: float,
                      O=None, W_state_out=None, X0_halo_out=None, workspace=None):
