@@ -94,3 +94,44 @@ def test_launch_counts():
     assert pkg.layer_launches(1, 2048, pkg.F32) == 6
     assert pkg.layer_launches(3, 0, pkg.BF16) == 1
     assert pkg.layer_launches(0, 100, pkg.BF16) == 0
+
+
+def _size(fn, *args):
+    lib = pkg.load()
+    out = ctypes.c_size_t(0)
+    st = getattr(lib, fn)(*args, ctypes.byref(out))
+    return st, out.value
+
+
+def test_training_buffer_sizes():
+    """The saved-activation buffer holds Z, [A | U], Y, V and every W_i (dtype) plus the counters;
+    the backward-from-saved workspace holds only the backward's own scratch, and the recomputing
+    backward's workspace is the two together."""
+    B, T, d, f, C, k = 2, 1000, 256, 512, 128, 4
+    a = lambda x: (x + 255) // 256 * 256
+    n = (T + C - 1) // C
+    st, saved = _size("ipttt_saved_size", B, T, d, f, C, k, pkg.BF16)
+    assert st == 0
+    assert saved == a(B * T * f * 2) + a(B * T * 2 * f * 2) + 2 * a(B * T * d * 2) + a(B * n * d * f * 2) + a(
+        (B * n + 1) * 4)
+    st, scratch = _size("ipttt_backward_saved_workspace_size", B, T, d, f, C, k, pkg.BF16)
+    strips = B * ((T + 63) // 64)
+    assert st == 0 and scratch == 2 * a(B * T * d * 2) + a(B * n * d * f * 2) + a(B * d * f * 4) + a(strips * d * k * 4)
+    st, full = _size("ipttt_backward_workspace_size", B, T, d, f, C, k, pkg.BF16)
+    assert st == 0 and full == saved + scratch
+    # fp32 adds dZ to the scratch
+    st, scratch32 = _size("ipttt_backward_saved_workspace_size", B, T, d, f, C, k, pkg.F32)
+    assert st == 0 and scratch32 == a(B * T * f * 4) + 2 * a(B * T * d * 4) + a(B * n * d * f * 4) + a(
+        B * d * f * 4) + a(strips * d * k * 4)
+    assert _size("ipttt_saved_size", 1, 64, 250, 512, 128, 4, pkg.BF16)[0] == 2  # d % 8
+
+
+def test_host_workspace_holds_one_piece():
+    """The host-buffer entry's workspace: the layer workspace for one piece (4096 tokens, a
+    multiple of C) plus whole H, X0, O, the fp32 state and two halos."""
+    B, T, d, f, C, k = 1, 32768, 2560, 9728, 1024, 4
+    st, host = _size("ipttt_host_workspace_size", B, T, d, f, C, k, pkg.BF16)
+    st2, piece = _size("ipttt_workspace_size", B, 4096, d, f, C, k, pkg.BF16)
+    a = lambda x: (x + 255) // 256 * 256
+    assert st == 0 and st2 == 0
+    assert host == piece + 3 * a(B * T * d * 2) + a(B * d * f * 4) + 2 * a(B * (k - 1) * d * 2)
