@@ -230,7 +230,7 @@ ipttt_status ipttt_backward_workspace_size(int64_t B, int64_t T, int64_t d, int6
  * bf16: every product on the tensor cores with fp32 accumulation; the intermediates (Z, V,
  * W_i, R_i, dA, dU, dV, dY) are rounded to bf16 between steps (dZ stays fp32: the SwiGLU
  * adjoints are taken in the epilogue of the GEMM that forms it).  B*T = 0 writes zeros
- * (dW_down0 = sum_b dW_final[b]).  Also requires B <= 65535 and T <= 524280.
+ * (dW_down0 = sum_b dW_final[b]).  Also requires B <= 65535 and T <= 2097120.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 ipttt_status ipttt_layer_backward(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
                                   const void* W_up, const void* W_down0, const void* W_target,

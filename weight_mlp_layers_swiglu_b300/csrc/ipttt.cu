@@ -991,6 +991,28 @@ ipttt_status run_forward_saved(ipttt_ctx* ctx, const void* H, const void* X0, co
   return run_state(ctx, sv.v, sv.z, W0, B, T, d, f, C, dt, sv.wst, W_fin_scratch, false);
 }
 
+// dX0 and the per-strip tap partials of the conv adjoint (kernels templated on the tap count).
+template <typename E>
+void launch_conv_adjoints(ipttt_ctx* ctx, dim3 gx, dim3 gw, const void* dY, const void* cw, const void* X0,
+                          void* dX0, float* part, int T_len, int d, int k) {
+  const E* dy = static_cast<const E*>(dY);
+  const E* w = static_cast<const E*>(cw);
+  const E* x = static_cast<const E*>(X0);
+  E* dx = static_cast<E*>(dX0);
+  const int sh = ctx->target_shift;
+  switch (k) {
+#define IPTTT_ADJ_CASE(KK)                                                                              \
+  case KK:                                                                                              \
+    simt::conv_backward_x_kernel<E, KK><<<gx, 64, 0, ctx->stream>>>(dy, w, dx, T_len, d, sh);           \
+    simt::conv_backward_w_partial_kernel<E, KK><<<gw, 64, 0, ctx->stream>>>(dy, x, part, T_len, d, sh); \
+    break;
+    IPTTT_ADJ_CASE(1) IPTTT_ADJ_CASE(2) IPTTT_ADJ_CASE(3) IPTTT_ADJ_CASE(4)
+    IPTTT_ADJ_CASE(5) IPTTT_ADJ_CASE(6) IPTTT_ADJ_CASE(7) IPTTT_ADJ_CASE(8)
+#undef IPTTT_ADJ_CASE
+    default: break;
+  }
+}
+
 // The backward pass from the saved forward activations (validated by the caller; T >= 1).  It
 // overwrites sv.au with [dA | dU].
 ipttt_status run_backward_core(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
@@ -1093,21 +1115,10 @@ ipttt_status run_backward_core(ipttt_ctx* ctx, const void* H, const void* X0, co
     const int64_t groups = d / (bf16 ? 8 : 4);  // 16-byte channel groups
     dim3 gx(ceil_div(groups, 64), ceil_div(T, simt::CONVX_ROWS), (unsigned)B);
     dim3 gw((unsigned)L.strips, ceil_div(groups, 64));
-    if (bf16) {
-      simt::conv_backward_x_kernel<__nv_bfloat16><<<gx, 64, 0, ctx->stream>>>(
-          static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(cw), static_cast<__nv_bfloat16*>(dX0),
-          (int)B, (int)T, (int)d, k, ctx->target_shift);
-      simt::conv_backward_w_partial_kernel<__nv_bfloat16><<<gw, 64, 0, ctx->stream>>>(
-          static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(X0), part, (int)B, (int)T, (int)d, k,
-          ctx->target_shift);
-    } else {
-      simt::conv_backward_x_kernel<float><<<gx, 64, 0, ctx->stream>>>(
-          static_cast<const float*>(dY), static_cast<const float*>(cw), static_cast<float*>(dX0), (int)B, (int)T,
-          (int)d, k, ctx->target_shift);
-      simt::conv_backward_w_partial_kernel<float><<<gw, 64, 0, ctx->stream>>>(
-          static_cast<const float*>(dY), static_cast<const float*>(X0), part, (int)B, (int)T, (int)d, k,
-          ctx->target_shift);
-    }
+    if (bf16)
+      launch_conv_adjoints<__nv_bfloat16>(ctx, gx, gw, dY, cw, X0, dX0, part, (int)T, (int)d, k);
+    else
+      launch_conv_adjoints<float>(ctx, gx, gw, dY, cw, X0, dX0, part, (int)T, (int)d, k);
     simt::sum_strips_kernel<<<ceil_div(d * k, 256), 256, 0, ctx->stream>>>(part, dcw, (int)L.strips, d * k);
     if ((s = check_launch(ctx, "conv backward launch")) != IPTTT_OK) return s;
   }

@@ -292,55 +292,76 @@ __global__ void swiglu_backward_kernel(const T* __restrict__ dZ, T* __restrict__
 }
 
 // Adjoint of the causal depthwise conv for its input: with the window shifted by `shift` tokens,
-// dX0[u, c] = sum_s w[c, s] dY[u - shift + (k-1) - s, c] over the rows that exist.  Grid:
-// x = blocks of 16-byte channel groups, y = blocks of CONVX_ROWS tokens, z = sequence; each
-// thread keeps its channels' taps in registers and produces CONVX_ROWS rows.
-constexpr int CONVX_ROWS = 8;
+// dX0[u, c] = sum_s w[c, s] dY[u - shift + (K-1) - s, c] over the rows that exist.  Grid:
+// x = blocks of 16-byte channel groups, y = blocks of CONVX_ROWS tokens, z = sequence.  Each
+// thread keeps its channels' taps and a sliding window of the last K dY rows in registers, so
+// it loads every dY row it needs once.
+constexpr int CONVX_ROWS = 32;
 
 template <typename T>
+__device__ __forceinline__ void load_row16(const T* p, bool ok, float (&v)[16 / sizeof(T)]) {
+  constexpr int VEC = 16 / sizeof(T);
+  uint4 raw = make_uint4(0, 0, 0, 0);
+  if (ok) raw = *reinterpret_cast<const uint4*>(p);
+  const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) v[j] = static_cast<float>(e[j]);
+}
+
+template <typename T, int K>
 __global__ void conv_backward_x_kernel(const T* __restrict__ dY, const T* __restrict__ conv_w, T* __restrict__ dX0,
-                                       int B, int T_len, int d, int k, int shift) {
+                                       int T_len, int d, int shift) {
   constexpr int VEC = 16 / sizeof(T);
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= d / VEC) return;
   const int c0 = g * VEC;
-  const int t0 = blockIdx.y * CONVX_ROWS;
-  const int64_t base = (int64_t)blockIdx.z * T_len;
-  float w[8][VEC];  // k <= 8
+  const int u0 = blockIdx.y * CONVX_ROWS;
+  const int u1 = min(u0 + CONVX_ROWS, T_len);
+  const T* dy = dY + (int64_t)blockIdx.z * T_len * d + c0;
+  T* dx = dX0 + (int64_t)blockIdx.z * T_len * d + c0;
+  float w[K][VEC];
 #pragma unroll
-  for (int s = 0; s < 8; ++s)
+  for (int s = 0; s < K; ++s)
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) w[s][j] = s < k ? static_cast<float>(conv_w[(int64_t)(c0 + j) * k + s]) : 0.f;
-  for (int t = t0; t < min(t0 + CONVX_ROWS, T_len); ++t) {
+    for (int j = 0; j < VEC; ++j) w[s][j] = static_cast<float>(conv_w[(int64_t)(c0 + j) * K + s]);
+  // win[m] = dY row u - shift + m (m = 0 .. K-1) for the current output row u
+  float win[K][VEC];
+#pragma unroll
+  for (int m = 1; m < K; ++m) {
+    const int r = u0 - shift + m - 1;
+    load_row16(dy + (int64_t)r * d, r >= 0 && r < T_len, win[m]);
+  }
+  for (int u = u0; u < u1; ++u) {
+#pragma unroll
+    for (int m = 0; m + 1 < K; ++m)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) win[m][j] = win[m + 1][j];
+    const int r = u - shift + K - 1;
+    load_row16(dy + (int64_t)r * d, r >= 0 && r < T_len, win[K - 1]);
     float acc[VEC];
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int src = t - shift + (k - 1) - s;
-      if (s >= k || src < 0 || src >= T_len) continue;
-      const uint4 raw = *reinterpret_cast<const uint4*>(dY + (base + src) * d + c0);
-      const T* v = reinterpret_cast<const T*>(&raw);
+    for (int s = 0; s < K; ++s)
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) acc[j] = fmaf(w[s][j], static_cast<float>(v[j]), acc[j]);
-    }
+      for (int j = 0; j < VEC; ++j) acc[j] = fmaf(w[s][j], win[K - 1 - s][j], acc[j]);
     uint4 out;
     T* o = reinterpret_cast<T*>(&out);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) o[j] = static_cast<T>(acc[j]);
-    *reinterpret_cast<uint4*>(dX0 + (base + t) * d + c0) = out;
+    *reinterpret_cast<uint4*>(dx + (int64_t)u * d) = out;
   }
 }
 
 // Adjoint for the taps, in two passes (deterministic): partial[strip, c, s] = sum over the strip's
-// tokens of dY[t, c] X0[t + shift - (k-1) + s, c]; then dconv_w[c, s] = sum over strips in order.
-// Grid: x = strip (B * ceil(T / CONVW_STRIP)), y = blocks of 16-byte channel groups.
+// tokens of dY[t, c] X0[t + shift - (K-1) + s, c]; then dconv_w[c, s] = sum over strips in order.
+// Grid: x = strip (B * ceil(T / CONVW_STRIP)), y = blocks of 16-byte channel groups.  A sliding
+// window of the last K X0 rows in registers: every row is loaded once per strip.
 constexpr int CONVW_STRIP = 64;
 
-template <typename T>
+template <typename T, int K>
 __global__ void conv_backward_w_partial_kernel(const T* __restrict__ dY, const T* __restrict__ X0,
-                                               float* __restrict__ partial, int B, int T_len, int d, int k,
-                                               int shift) {
+                                               float* __restrict__ partial, int T_len, int d, int shift) {
   constexpr int VEC = 16 / sizeof(T);
   const int g = blockIdx.y * blockDim.x + threadIdx.x;
   if (g >= d / VEC) return;
@@ -352,31 +373,37 @@ __global__ void conv_backward_w_partial_kernel(const T* __restrict__ dY, const T
   const int t1 = min(t0 + CONVW_STRIP, T_len);
   const T* dy = dY + (int64_t)b * T_len * d + c0;
   const T* x = X0 + (int64_t)b * T_len * d + c0;
-  float acc[8][VEC];  // k <= 8
+  float acc[K][VEC];
 #pragma unroll
-  for (int s = 0; s < 8; ++s)
+  for (int s = 0; s < K; ++s)
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[s][j] = 0.f;
-#pragma unroll 4
-  for (int t = t0; t < t1; ++t) {
-    const uint4 rd = *reinterpret_cast<const uint4*>(dy + (int64_t)t * d);
-    const T* dv = reinterpret_cast<const T*>(&rd);
+  // win[s] = X0 row t + shift - (K-1) + s for the current token t
+  float win[K][VEC];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int src = t + shift - (k - 1) + s;
-      if (s >= k || src < 0 || src >= T_len) continue;
-      const uint4 rx = *reinterpret_cast<const uint4*>(x + (int64_t)src * d);
-      const T* xv = reinterpret_cast<const T*>(&rx);
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) acc[s][j] = fmaf(static_cast<float>(dv[j]), static_cast<float>(xv[j]), acc[s][j]);
-    }
+  for (int s = 1; s < K; ++s) {
+    const int r = t0 + shift - K + s;
+    load_row16(x + (int64_t)r * d, r >= 0 && r < T_len, win[s]);
   }
-  float* out = partial + ((int64_t)strip * d + c0) * k;
+  for (int t = t0; t < t1; ++t) {
+#pragma unroll
+    for (int s = 0; s + 1 < K; ++s)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) win[s][j] = win[s + 1][j];
+    const int r = t + shift;
+    load_row16(x + (int64_t)r * d, r >= 0 && r < T_len, win[K - 1]);
+    float dv[VEC];
+    load_row16(dy + (int64_t)t * d, true, dv);
+#pragma unroll
+    for (int s = 0; s < K; ++s)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) acc[s][j] = fmaf(dv[j], win[s][j], acc[s][j]);
+  }
+  float* out = partial + ((int64_t)strip * d + c0) * K;
 #pragma unroll
   for (int j = 0; j < VEC; ++j)
 #pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (s < k) out[j * k + s] = acc[s][j];
+    for (int s = 0; s < K; ++s) out[j * K + s] = acc[s][j];
 }
 
 __global__ void sum_strips_kernel(const float* __restrict__ partial, float* __restrict__ out, int strips, int64_t n) {
