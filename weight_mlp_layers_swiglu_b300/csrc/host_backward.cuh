@@ -84,7 +84,7 @@ ipttt_status launch_two_seg(ipttt_ctx* ctx, const void* A1, int64_t a1_stride, c
   p.st = dev_status(ctx);
   const int tiles = p.problems * p.m_tiles * p.n_tiles;
   if (pairs) {
-    p.group_m = 8;
+    p.group_m = b_per_problem ? 8 : 32;  // one shared B (dH): as the SwiGLU GEMM
     gemm2::tc_gemm2_kernel<gemm::kTwoSeg><<<pair_grid(ctx, tiles), gemm2::NUM_THREADS, gemm2::SMEM_BYTES,
                                            ctx->stream>>>(ma1, mb1, ma2, mo, mb2, p);
   } else {
@@ -137,7 +137,7 @@ ipttt_status run_swiglu_save(ipttt_ctx* ctx, const void* H, const void* Wg, cons
     p.n_tiles = ceil_div(f, 128);
     p.k_blocks = ceil_div(d, gemm::BK);
     p.problems = 1;
-    p.group_m = pairs ? 8 : 16;
+    p.group_m = pairs ? 32 : 16;  // as the SwiGLU GEMM of the forward
     p.scale = 1.f;
     p.st = dev_status(ctx);
     const int tiles = p.m_tiles * p.n_tiles;
