@@ -339,11 +339,36 @@ def stream_leg(args, w, ctx, weights, H, X0, dev, world):
     one_pass()
     passes = 5
     ms = sum(one_pass() for _ in range(passes)) / passes
+
+    # decoding: one token per call, the C-token buffer committing each chunk's update when it
+    # completes (the first chunk of the sequence, token by token)
+    n_dec = min(w.C, w.T)
+    Hd = [H[:, t:t + 1].contiguous() for t in range(n_dec)]
+    Xd = [X0[:, t:t + 1].contiguous() for t in range(n_dec)]
+
+    def decode_pass():
+        sl = pkg.StreamingLayer(ctx, weights["W_gate"], weights["W_up"], weights["W_down0"], weights["W_target"],
+                                weights["conv_w"], w.B, w.C, w.eta)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for h, x in zip(Hd, Xd):
+            sl.step(h, x)
+        sl.flush()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    decode_pass()
+    ms_dec = min(decode_pass() for _ in range(3))
     if ctx.sync() != 0:
         raise RuntimeError(f"device status in the streaming leg: {ctx.last_error()}")
     ms = max_over_ranks(ms, world, dev)
+    ms_dec = max_over_ranks(ms_dec, world, dev)
     return {"call_tokens": S, "calls_per_sequence": len(cuts), "value": w.B * w.T * world / (ms * 1e-3),
-            "unit": UNIT, "ms_per_sequence": ms}
+            "unit": UNIT, "ms_per_sequence": ms,
+            "decode": {"tokens_per_call": 1, "tokens": n_dec, "value": w.B * n_dec * world / (ms_dec * 1e-3),
+                       "unit": UNIT, "ms_per_token": ms_dec / n_dec}}
 
 
 def run_cp(args, w):

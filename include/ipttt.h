@@ -194,6 +194,14 @@ ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const 
                                       ipttt_dtype dtype, void* O_host, float* W_final_host,
                                       void* workspace, size_t workspace_bytes);
 
+/* The weight a chunk is applied with, from a running fp32 state (the decode path of a stream:
+ * tokens of a chunk that is not complete yet are applied with the weight at the chunk's start,
+ * §3.2 Step 3): W[b] = W_state[b] rounded to dtype (bf16 round to nearest even; fp32 copies).
+ * W_state [B, d, d_ff] fp32, W [B, d, d_ff] dtype, both device; they must not overlap.
+ * Errors: INVALID_ARG, UNSUPPORTED (as ipttt_workspace_size for d, d_ff, dtype), CUDA. */
+ipttt_status ipttt_state_weight(ipttt_ctx* ctx, const float* W_state, int64_t B, int64_t d, int64_t d_ff,
+                                ipttt_dtype dtype, void* W);
+
 /* ---- backward pass ----
  * The pages train the layer (§5 results: continued training of a 4B model, experiment 1, and
  * pretraining from scratch, experiment 3) but print no gradient formulas; these are the exact

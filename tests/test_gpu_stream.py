@@ -62,6 +62,7 @@ def test_stream_cut_at_chunk_multiples_is_bit_exact(ctx, fused, dt, cuts):
         outs = []
         for lo, hi in zip([0] + cuts, cuts + [w.T]):
             outs.append(sl.step(xd["H"][:, lo:hi].contiguous(), xd["X0"][:, lo:hi].contiguous()))
+        sl.flush()  # the sequence ends inside a chunk: commit that chunk's update
         assert ctx.sync() == 0, ctx.last_error()
     finally:
         ctx.set_fused_tail(True)
@@ -105,3 +106,40 @@ def test_resume_rejects_overlapping_halo(ctx):
         ctx.layer_resume(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], W_state, halo,
                          128, 0.1, X0_halo_out=halo)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("dt,B,T,d,f,C,steps", [
+    ("bf16", 2, 300, 128, 256, 128, [1] * 300),                    # token-by-token decoding
+    ("bf16", 1, 700, 256, 512, 256, [1, 5, 250, 3, 2, 256, 100, 83]),  # mixed calls, CTA-pair chunks
+    ("bf16", 2, 520, 128, 256, 128, [256, 1, 1, 1, 125, 136]),     # prefill, then decode
+    ("f32", 2, 200, 64, 128, 48, [7, 1, 40, 52, 100]),
+])
+def test_decode_with_chunk_buffer_matches_one_call(ctx, dt, B, T, d, f, C, steps):
+    """Calls of any length: tokens of an incomplete chunk are applied with the weight at the
+    chunk's start and the chunk's update is committed when it completes; outputs, and after
+    flush() the final state, equal one call over the whole sequence bit for bit."""
+    import weight_mlp_layers_swiglu_b300 as pkg
+
+    assert sum(steps) == T
+    w, x = random_case(B, T, d, f, C, 4, 4.0 / C, dt, 90 + T)
+    xd = to_dev(x)
+    O_ref, W_ref = ctx.layer_forward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
+                                     xd["conv_w"], C, w.eta)
+    O_ref, W_ref = O_ref.clone(), W_ref.clone()
+    sl = pkg.StreamingLayer(ctx, xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"], xd["conv_w"], B, C, w.eta)
+    outs, lo = [], 0
+    for n in steps:
+        outs.append(sl.step(xd["H"][:, lo:lo + n].contiguous(), xd["X0"][:, lo:lo + n].contiguous()))
+        lo += n
+    sl.flush()
+    assert ctx.sync() == 0, ctx.last_error()
+    assert torch.equal(torch.cat(outs, dim=1), O_ref)
+    assert torch.equal(sl.state, W_ref)
+
+
+def test_state_weight_rounds_the_state(ctx):
+    W_state = seeded((2, 64, 128), 1.0, torch.float32, 91, "cuda")
+    W = ctx.state_weight(W_state, torch.bfloat16)
+    W32 = ctx.state_weight(W_state, torch.float32)
+    assert ctx.sync() == 0
+    assert torch.equal(W, W_state.to(torch.bfloat16)) and torch.equal(W32, W_state)

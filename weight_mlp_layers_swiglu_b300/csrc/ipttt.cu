@@ -610,6 +610,33 @@ ipttt_status ipttt_chunk_apply(ipttt_ctx* ctx, const void* Z, const void* W_eff,
   return run_apply(ctx, Z, W_eff, B, T, d, d_ff, C, dt, O);
 }
 
+ipttt_status ipttt_state_weight(ipttt_ctx* ctx, const float* W_state, int64_t B, int64_t d, int64_t d_ff,
+                                ipttt_dtype dt, void* W) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, B, 1, d, d_ff, 1, 1, dt, false);
+  if (s != IPTTT_OK) return s;
+  if (B == 0) return IPTTT_OK;
+  if (!W_state || !W || !aligned16(W_state) || !aligned16(W)) {
+    set_err(ctx, "state_weight: NULL or misaligned pointer");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  const int64_t n = B * d * d_ff;
+  std::vector<Region> all = {{W_state, (size_t)n * 4, "W_state"}, {W, (size_t)n * esize(dt), "W"}};
+  std::vector<Region> outs = {all[1]};
+  std::string what;
+  if (find_overlap(outs, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  if (dt == IPTTT_BF16)
+    simt::state_weight_kernel<__nv_bfloat16><<<ceil_div(n, 256), 256, 0, ctx->stream>>>(
+        W_state, static_cast<__nv_bfloat16*>(W), n);
+  else
+    simt::state_weight_kernel<float><<<ceil_div(n, 256), 256, 0, ctx->stream>>>(W_state, static_cast<float*>(W), n);
+  return check_launch(ctx, "state weight launch");
+}
+
 ipttt_status ipttt_timing_begin(ipttt_ctx* ctx) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
   ctx->timing = true;

@@ -422,6 +422,14 @@ __global__ void broadcast_state_kernel(const T* __restrict__ W0, float* __restri
   if (e < df) W_final[(int64_t)blockIdx.y * df + e] = static_cast<float>(W0[e]);
 }
 
+// The weight a chunk is applied with, from the running fp32 state: W[e] = T(state[e]) (bf16
+// round to nearest even, or an fp32 copy).
+template <typename T>
+__global__ void state_weight_kernel(const float* __restrict__ state, T* __restrict__ W, int64_t n) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < n) W[e] = static_cast<T>(state[e]);
+}
+
 // Device-side wait that nothing ever signals: exercises the bounded-wait path.
 __global__ void wait_probe_kernel(DevStatus st) {
   __shared__ __align__(8) uint64_t bar;

@@ -60,6 +60,7 @@ _SIGNATURES = {
     "ipttt_layer_backward_saved": (ctypes.c_int, [c_vp] * 7 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                                                              c_vp, ctypes.c_size_t] + [c_vp] * 10
                                    + [ctypes.c_size_t]),
+    "ipttt_state_weight": (ctypes.c_int, [c_vp, c_vp] + [c_i64] * 3 + [ctypes.c_int, c_vp]),
     "ipttt_swiglu": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, c_vp]),
     "ipttt_target": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_int, c_vp, c_vp]),
     "ipttt_chunk_state": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 5 + [ctypes.c_int, c_vp, c_vp]),
@@ -405,6 +406,16 @@ class Context:
         self._check(st, "layer_forward_host")
         return O_host, W_final_host
 
+    def state_weight(self, W_state, dtype, W=None):
+        """The chunk weight from an fp32 state [B, d, d_ff]: W_state rounded to `dtype`."""
+        B, d, f = W_state.shape
+        _need(W_state, "W_state", (B, d, f), torch.float32, self.device)
+        W = W if W is not None else torch.empty((B, d, f), dtype=dtype, device=self.device)
+        _need(W, "W", (B, d, f), dtype, self.device)
+        self._check(self.lib.ipttt_state_weight(self.h, _ptr(W_state), B, d, f, dtype_code(dtype), _ptr(W)),
+                    "state_weight")
+        return W
+
     # ------------------------------------------------------------------ the steps
     def swiglu(self, H2d, W_gate, W_up, Z=None):
         rows, d = H2d.shape
@@ -483,23 +494,74 @@ class Context:
 class StreamingLayer:
     """Keeps the per-sequence fast-weight state and conv halo of B sequences across calls.
 
-    Each call to step() runs the layer on the next tokens of every sequence, continuing from the
-    state the previous call left; cutting a sequence at multiples of C gives exactly the results
-    of one call over the whole sequence.  Buffers only: all compute runs in the library.
+    step() takes any number of tokens per call (one token at a time for decoding):
+      * whole chunks starting at a chunk boundary run through the resumable layer;
+      * tokens of a chunk that is not complete yet are applied at once with the weight at the
+        chunk's start (Z from the SwiGLU step, then the chunk apply with that weight), and their
+        inputs are buffered; when the chunk completes, its update is committed by running the
+        resumable layer over the buffered chunk (the C-token buffer of a decode loop).
+    Every output and the state after every complete chunk equal those of one call over the whole
+    sequence bit for bit.  flush() commits a final partial chunk, after which `state` is the
+    final W_down of the whole sequence.  Buffers only: all compute runs in the library.
     """
 
     def __init__(self, ctx: Context, W_gate, W_up, W_down0, W_target, conv_w, B: int, C: int, eta: float):
-        self.ctx, self.C, self.eta = ctx, C, eta
+        self.ctx, self.C, self.eta, self.B = ctx, C, eta, B
         self.W_gate, self.W_up, self.W_target, self.conv_w = W_gate, W_up, W_target, conv_w
         d, f = W_down0.shape
         k = conv_w.shape[1]
-        self.state = W_down0.float().unsqueeze(0).expand(B, d, f).contiguous()
-        self.halo = torch.zeros((B, k - 1, d), dtype=W_down0.dtype, device=W_down0.device)
+        dt, dev = W_down0.dtype, W_down0.device
+        self.d, self.f, self.dtype = d, f, dt
+        empty = torch.empty((B, 0, d), dtype=dt, device=dev)
+        # an empty call leaves every sequence's state at W_down0 (fp32)
+        _, self.state = ctx.layer_forward(empty, empty, W_gate, W_up, W_down0, W_target, conv_w, C, eta)
+        self.state = self.state.clone()
+        self.halo = torch.zeros((B, k - 1, d), dtype=dt, device=dev)
         self._halo_next = torch.empty_like(self.halo)
+        self.W_cur = ctx.state_weight(self.state, dt)  # the weight of the current chunk
+        self.pending = 0  # tokens of the current chunk already seen
+        self._pend_H = torch.empty((B, C, d), dtype=dt, device=dev)
+        self._pend_X = torch.empty((B, C, d), dtype=dt, device=dev)
 
-    def step(self, H, X0, O=None):
+    def _resume(self, H, X0, O=None):
         O, self.state, self._halo_next = self.ctx.layer_resume(
             H, X0, self.W_gate, self.W_up, self.W_target, self.conv_w, self.state, self.halo, self.C, self.eta,
             O=O, W_state_out=self.state, X0_halo_out=self._halo_next)
         self.halo, self._halo_next = self._halo_next, self.halo
+        self.ctx.state_weight(self.state, self.dtype, self.W_cur)
         return O
+
+    def _commit_pending(self):
+        n = self.pending
+        self._resume(self._pend_H[:, :n].contiguous(), self._pend_X[:, :n].contiguous())
+        self.pending = 0
+
+    def step(self, H, X0, O=None):
+        B, n, d = H.shape
+        outs, pos = [], 0
+        while pos < n:
+            if self.pending == 0 and n - pos >= self.C:
+                m = (n - pos) // self.C * self.C
+                outs.append(self._resume(H[:, pos:pos + m].contiguous(), X0[:, pos:pos + m].contiguous()))
+                pos += m
+                continue
+            m = min(self.C - self.pending, n - pos)
+            h = H[:, pos:pos + m].contiguous()
+            Z = self.ctx.swiglu(h.view(B * m, d), self.W_gate, self.W_up)
+            outs.append(self.ctx.chunk_apply(Z.view(B, m, self.f), self.W_cur.view(B, 1, d, self.f), self.C))
+            self._pend_H[:, self.pending:self.pending + m] = h
+            self._pend_X[:, self.pending:self.pending + m] = X0[:, pos:pos + m]
+            self.pending += m
+            pos += m
+            if self.pending == self.C:
+                self._commit_pending()
+        out = outs[0] if len(outs) == 1 else torch.cat(outs, dim=1)
+        if O is not None:
+            O.copy_(out)
+            return O
+        return out
+
+    def flush(self):
+        """Commit the update of a final partial chunk (the stream ends inside a chunk)."""
+        if self.pending:
+            self._commit_pending()
