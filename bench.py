@@ -673,14 +673,19 @@ def dominant_traffic(kernel: str, w):
     return entry.get("bytes_per_launch")
 
 
+# The sources a tensor-core kernel's DRAM traffic depends on: the kernels themselves and the
+# launch configurations (tiles, rasterisation, grids) in the step launchers.
+TRAFFIC_SOURCES = ("ptx.cuh", "tc_gemm.cuh", "tc_gemm2.cuh", "tc_state.cuh", "tc_state2.cuh", "tc_fused.cuh",
+                   "tc_fused2.cuh", "host_steps.cuh")
+
+
 def source_digest(src_dir: str) -> str:
     import hashlib
 
     h = hashlib.sha256()
-    for f in sorted(os.listdir(src_dir)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(src_dir, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(src_dir, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
