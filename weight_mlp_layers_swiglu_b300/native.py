@@ -518,7 +518,8 @@ class StreamingLayer:
         self.state = self.state.clone()
         self.halo = torch.zeros((B, k - 1, d), dtype=dt, device=dev)
         self._halo_next = torch.empty_like(self.halo)
-        self.W_cur = ctx.state_weight(self.state, dt)  # the weight of the current chunk
+        self.W_cur = torch.empty((B, d, f), dtype=dt, device=dev)  # the weight of the current chunk
+        self._w_cur_ok = False  # W_cur holds the weight of the current state
         self.pending = 0  # tokens of the current chunk already seen
         self._pend_H = torch.empty((B, C, d), dtype=dt, device=dev)
         self._pend_X = torch.empty((B, C, d), dtype=dt, device=dev)
@@ -528,7 +529,7 @@ class StreamingLayer:
             H, X0, self.W_gate, self.W_up, self.W_target, self.conv_w, self.state, self.halo, self.C, self.eta,
             O=O, W_state_out=self.state, X0_halo_out=self._halo_next)
         self.halo, self._halo_next = self._halo_next, self.halo
-        self.ctx.state_weight(self.state, self.dtype, self.W_cur)
+        self._w_cur_ok = False
         return O
 
     def _commit_pending(self):
@@ -546,6 +547,9 @@ class StreamingLayer:
                 pos += m
                 continue
             m = min(self.C - self.pending, n - pos)
+            if not self._w_cur_ok:  # first tokens of a chunk: its weight, from the state
+                self.ctx.state_weight(self.state, self.dtype, self.W_cur)
+                self._w_cur_ok = True
             h = H[:, pos:pos + m].contiguous()
             Z = self.ctx.swiglu(h.view(B * m, d), self.W_gate, self.W_up)
             outs.append(self.ctx.chunk_apply(Z.view(B, m, self.f), self.W_cur.view(B, 1, d, self.f), self.C))
