@@ -90,7 +90,7 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   if ((e = cudaStreamWaitEvent(ctx->stream, ctx->join, 0)) != cudaSuccess) return cuda_fail(ctx, e, "join");
   mark(ctx, call, kEvJoined, ctx->stream);
   const bool bf16 = dt == IPTTT_BF16;  // W_eff[b, 0] = W_down0: the apply reads W_down0 itself
-  const bool fuse = bf16 && ctx->fused_tail && ctx->coop;
+  bool fuse = bf16 && ctx->fused_tail && ctx->coop;
   uint32_t* ctr = sv ? sv->ctr : reinterpret_cast<uint32_t*>(base + L.ctr);
   const int n_ctr = (int)(B * n_chunks_of(T, C) + 1);
   if (Wt != nullptr) {
@@ -102,13 +102,18 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
   }
   mark(ctx, call, kEvTargetEnd, ctx->stream);
   if (fuse) {
-    if ((s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr, W_init, sv != nullptr)) !=
-        IPTTT_OK)
+    s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr, W_init, sv != nullptr);
+    if (s == IPTTT_ERR_UNSUPPORTED) {
+      fuse = false;  // the cooperative launch was refused: separate kernels below
+    } else if (s != IPTTT_OK) {
       return s;
-    mark(ctx, call, kEvStateEnd, ctx->stream);
-    mark(ctx, call, kEvApplyEnd, ctx->stream);
-    if (call >= 0) ctx->timed_fused[call] = 1;
-  } else {
+    } else {
+      mark(ctx, call, kEvStateEnd, ctx->stream);
+      mark(ctx, call, kEvApplyEnd, ctx->stream);
+      if (call >= 0) ctx->timed_fused[call] = 1;
+    }
+  }
+  if (!fuse) {
     const bool skip_first = bf16 && sv == nullptr;  // the training forward keeps W_0 in the stack too
     if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, skip_first, W_init)) != IPTTT_OK) return s;
     mark(ctx, call, kEvStateEnd, ctx->stream);

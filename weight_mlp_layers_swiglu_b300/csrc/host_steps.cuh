@@ -323,7 +323,9 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
       cudaLaunchKernelEx(&cfg, fused2::tc_state_apply2_kernel, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
   if (e != cudaSuccess) {
     cudaGetLastError();  // a refused launch configuration is not sticky
-    ctx->fused_pairs = false;
+    // "too large": other work holds SMs right now; anything else: the driver does not take
+    // cooperative launches of clusters, so stop trying
+    if (e != cudaErrorCooperativeLaunchTooLarge) ctx->fused_pairs = false;
     return false;
   }
   *st = check_launch(ctx, "state+apply launch");
@@ -389,6 +391,12 @@ ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z,
   cfg.numAttrs = 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, fused::tc_state_apply_kernel, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    // the SMs are not all free for this launch (another kernel runs beside it): the caller
+    // runs steps (3)-(5) as separate kernels instead
+    cudaGetLastError();
+    return IPTTT_ERR_UNSUPPORTED;
+  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "state+apply launch");
   return check_launch(ctx, "state+apply launch");
 }
