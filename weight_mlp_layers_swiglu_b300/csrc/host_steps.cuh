@@ -323,8 +323,9 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
       cudaLaunchKernelEx(&cfg, fused2::tc_state_apply2_kernel, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
   if (e != cudaSuccess) {
     cudaGetLastError();  // a refused launch configuration is not sticky
-    // "too large": other work holds SMs right now; anything else: the driver does not take
-    // cooperative launches of clusters, so stop trying
+    // "too large": this context now has fewer SMs than the grid was sized for (the next call
+    // may fit again); anything else: the driver does not take cooperative launches of
+    // clusters, so stop trying
     if (e != cudaErrorCooperativeLaunchTooLarge) ctx->fused_pairs = false;
     return false;
   }
@@ -392,8 +393,8 @@ ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z,
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, fused::tc_state_apply_kernel, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
-    // the SMs are not all free for this launch (another kernel runs beside it): the caller
-    // runs steps (3)-(5) as separate kernels instead
+    // more CTAs than this context can hold at once (fewer SMs than at sizing time): the
+    // caller runs steps (3)-(5) as separate kernels instead
     cudaGetLastError();
     return IPTTT_ERR_UNSUPPORTED;
   }
