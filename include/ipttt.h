@@ -78,9 +78,10 @@ const char* ipttt_version(void);
 const char* ipttt_status_string(ipttt_status s);
 
 /* Create a context on CUDA device `device`, bound to `cuda_stream` (a cudaStream_t; NULL =
- * the legacy default stream).  Allocates a 8-byte device status word, CUDA events and one
- * internal side stream (ordered after and joined back into the context's stream by events);
- * this is the only call that allocates device memory.  *out receives the context.
+ * the legacy default stream).  Allocates a 8-byte device status word, CUDA events and three
+ * internal streams (the causal conv's side stream, and the upload and download streams of
+ * ipttt_layer_forward_host), each ordered after and joined back into the context's stream by
+ * events; this is the only call that allocates device memory.  *out receives the context.
  * Errors: INVALID_ARG (out == NULL, bad device), CUDA. */
 ipttt_status ipttt_create(ipttt_ctx** out, int device, void* cuda_stream);
 
@@ -91,7 +92,8 @@ ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* cuda_stream);
  * run first and the per-chunk apply tiles fill the SMs the state work leaves idle (each tile
  * waits on device-side counters until the weights of its chunk are written).  enable = 0
  * selects two separate kernels instead (same results, bit for bit); devices without
- * cooperative launch always use two. */
+ * cooperative launch, and calls whose cooperative grid no longer fits the SMs available to the
+ * context, use two. */
 ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable);
 
 /* Choose how the bf16 GEMMs of steps (1), (2) and (5) run: enable = 1 (default) on CTA pairs
