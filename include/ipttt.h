@@ -173,6 +173,26 @@ ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const voi
                                         ipttt_dtype dtype, void* O, float* W_state_out, void* X0_halo_out,
                                         void* workspace, size_t workspace_bytes);
 
+/* ---- context parallelism: the pages' three steps (§3.2) on one rank ----
+ * Step 1, ipttt_layer_totals: for a rank's range of tokens of every sequence (the conv
+ * continuing from X0_halo, the k-1 X0 rows before the range, NULL = zeros), Z and V go to
+ * `saved` (the ipttt_saved_size() layout) and S[b] = eta * sum_i V_i^T Z_i [B, d, d_ff] fp32
+ * is the range's update total, accumulated from zero with no per-chunk weight written.
+ * Step 2 is the caller's exchange: the rank's starting state is W_down0 plus the totals of
+ * the ranks before it.  Step 3, ipttt_layer_apply_saved: from that state W_init [B, d, d_ff]
+ * fp32 and the same `saved`, O [B, T, d] and the state after the range W_final [B, d, d_ff]
+ * fp32 (W_final may be W_init itself); Z and V are not computed again.  Errors as the layer
+ * calls. */
+ipttt_status ipttt_layer_totals(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                                const void* W_up, const void* W_target, const void* conv_w,
+                                const void* X0_halo, int64_t B, int64_t T, int64_t d, int64_t d_ff,
+                                int64_t C, int k, float eta, ipttt_dtype dtype, float* S, void* saved,
+                                size_t saved_bytes);
+
+ipttt_status ipttt_layer_apply_saved(ipttt_ctx* ctx, const float* W_init, int64_t B, int64_t T,
+                                     int64_t d, int64_t d_ff, int64_t C, ipttt_dtype dtype, void* saved,
+                                     size_t saved_bytes, void* O, float* W_final);
+
 /* Bytes of device workspace ipttt_layer_forward_host needs: ipttt_workspace_size() for one
  * piece (see below), then device staging for the whole H, X0 and O, the fp32 state [B,d,d_ff]
  * and two conv halos [B,k-1,d]. */

@@ -135,3 +135,61 @@ def test_host_workspace_holds_one_piece():
     a = lambda x: (x + 255) // 256 * 256
     assert st == 0 and st2 == 0
     assert host == piece + 3 * a(B * T * d * 2) + a(B * d * f * 4) + 2 * a(B * (k - 1) * d * 2)
+
+
+
+def _declarations():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for m in re.finditer(r"([A-Za-z_][\w \*]*?)\b(ipttt_[a-z_]+)\s*\(([^)]*)\)\s*;", text):
+        params = [" ".join(p.split()) for p in m.group(3).split(",")]
+        yield m.group(2), m.group(1).strip(), [] if params == ["void"] else params
+
+
+def _c_kind(decl: str):
+    """The kind of value a C parameter (with its name) or return type carries."""
+    stars = decl.count("*")
+    words = [w for w in decl.replace("*", " ").split() if w != "const"]
+    base = words[0]
+    if stars >= 2:
+        return "ptrptr"
+    if stars == 1:
+        return {"char": "char_p", "size_t": "size_p"}.get(base, "ptr")
+    return {"int64_t": "i64", "uint64_t": "u64", "int": "i32", "ipttt_dtype": "i32", "ipttt_status": "i32",
+            "float": "f32", "double": "f64", "size_t": "size", "void": None}[base]
+
+
+def _ctypes_kind(t):
+    if t is None:
+        return None
+    if t is ctypes.c_char_p:
+        return "char_p"
+    if t is ctypes.c_void_p:
+        return "ptr"
+    if t is ctypes.POINTER(ctypes.c_void_p):
+        return "ptrptr"
+    if t is ctypes.POINTER(ctypes.c_size_t):
+        return "size_p"
+    if isinstance(t, type) and issubclass(t, ctypes._Pointer):
+        return "ptr"
+    return {ctypes.c_int64: "i64", ctypes.c_uint64: "u64", ctypes.c_int: "i32", ctypes.c_float: "f32",
+            ctypes.c_double: "f64", ctypes.c_size_t: "size"}[t]
+
+
+def test_binding_signatures_match_the_header():
+    """Every argument the binding marshals has the width and kind the header declares, so a
+    shifted or missing argument fails here rather than on the device."""
+    sigs = native._SIGNATURES
+    decls = {name: (ret, params) for name, ret, params in _declarations()}
+    assert set(sigs) <= set(decls)
+    for name, (restype, argtypes) in sigs.items():
+        ret, params = decls[name]
+        want = [_c_kind(p) for p in params]
+        got = [_ctypes_kind(t) for t in argtypes]
+        assert len(got) == len(want), (name, len(got), len(want))
+        for i, (g, w) in enumerate(zip(got, want)):
+            # A size_t* result may be passed as a plain address; size_t and uint64_t are one
+            # ctypes type on this platform.
+            w = "u64" if w == "size" else w
+            g = "u64" if g == "size" else g
+            assert g == w or (w == "size_p" and g == "ptr"), (name, i, params[i], g)
+        assert _ctypes_kind(restype) == _c_kind(ret), (name, ret)

@@ -33,3 +33,31 @@ def test_emulated_ranks_match_one_call(dt, world, T_r):
                                       x["conv_w"], w.C, w.eta)
     assert rel_err(O, O_or) <= TOL[dt] and rel_err(W, W_or) <= TOL[dt]
     assert rel_err(O, O_ref) <= TOL[dt] and rel_err(W, W_ref) <= TOL[dt] / 20
+
+
+@pytest.mark.parametrize("dt,B,T,d,f,C,k", [("bf16", 2, 700, 256, 512, 256, 4), ("bf16", 1, 300, 192, 384, 128, 3),
+                                          ("f32", 2, 200, 64, 128, 48, 4)])
+def test_totals_and_apply_saved_match_resume(dt, B, T, d, f, C, k):
+    """Step 1 (the update total from zero, Z and V kept) equals the final state of a resumed call
+    from zero, and Step 3 from the kept Z and V equals the resumed call from the same state, bit
+    for bit."""
+    import weight_mlp_layers_swiglu_b300 as pkg
+    from tests.util import seeded
+
+    w, x = random_case(B, T, d, f, C, k, 2.0 / C, dt, 93)
+    xd = to_dev(x)
+    ctx = pkg.Context(0)
+    halo = seeded((B, k - 1, d), 0.02, x["H"].dtype, 94, "cuda")
+    zero = torch.zeros((B, d, f), dtype=torch.float32, device="cuda")
+    _, S_ref, _ = ctx.layer_resume(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], zero,
+                                   halo, C, w.eta)
+    S, saved = ctx.layer_totals(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], halo, C,
+                                w.eta)
+    W_init = (seeded((B, d, f), f ** -0.5, torch.float32, 95) + x["W_down0"].float()).cuda()
+    O_ref, W_ref, _ = ctx.layer_resume(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"],
+                                       W_init, halo, C, w.eta)
+    O, Wf = ctx.layer_apply_saved(W_init, T, C, saved, x["H"].dtype)
+    assert ctx.sync() == 0, ctx.last_error()
+    assert torch.equal(S, S_ref)
+    assert torch.equal(O, O_ref) and torch.equal(Wf, W_ref)
+    ctx.close()

@@ -95,17 +95,24 @@ def cp_forward_emulated(H, X0, W_down0, k: int, world: int, T_r: int, local_tota
 def library_locals(ctx, W_gate, W_up, W_target, conv_w, C: int, eta: float):
     """local_total / local_resume backed by the CUDA library (a Context on this rank's GPU).
 
-    local_total runs the resumable layer from a zero state, whose final state is the rank's
-    update total (its output is not used)."""
+    local_total is Step 1 (ipttt_layer_totals): the range's update total from a zero state, with
+    the range's Z and V kept; local_resume is Step 3 (ipttt_layer_apply_saved) from those, so Z
+    and V are computed once per range.  The Step 3 calls take the kept ranges in the order of
+    the Step 1 calls (one range per rank; the ranks emulated one after another in one process
+    run all their Step 1 calls first, in rank order)."""
+    from collections import deque
+
+    saved = deque()
 
     def local_total(H_r, X0_r, halo):
-        B, _, d = H_r.shape
-        zero = torch.zeros((B, d, W_gate.shape[0]), dtype=torch.float32, device=H_r.device)
-        _, S, _ = ctx.layer_resume(H_r, X0_r, W_gate, W_up, W_target, conv_w, zero, halo, C, eta)
+        S, buf = ctx.layer_totals(H_r, X0_r, W_gate, W_up, W_target, conv_w, halo, C, eta)
+        saved.append((H_r.shape[1], buf))
         return S
 
     def local_resume(H_r, X0_r, W_init, halo):
-        O, W_fin, _ = ctx.layer_resume(H_r, X0_r, W_gate, W_up, W_target, conv_w, W_init.contiguous(), halo, C, eta)
-        return O, W_fin
+        T_r, buf = saved.popleft()
+        if T_r != H_r.shape[1]:
+            raise ValueError("Step 3 range does not match the Step 1 range kept first")
+        return ctx.layer_apply_saved(W_init.contiguous(), T_r, C, buf, H_r.dtype)
 
     return local_total, local_resume

@@ -11,6 +11,76 @@ void mark(ipttt_ctx* ctx, int call, int which, cudaStream_t stream) {
   if (call >= 0) cudaEventRecord(ctx->events[(size_t)call * kEventsPerCall + which], stream);
 }
 
+// Steps (3)-(5) from V (eta-scaled) and Z: the fused cooperative kernel when *fuse (its
+// counters `ctr` already cleared), else, or when its launch is refused, the state kernel and the
+// apply; *fuse tells which ran.  W_init (optional) is each sequence's starting state, else W0;
+// write_first keeps W_0 in the stack Wst too (else chunk 0 reads W0 itself when W_init is NULL).
+ipttt_status run_tail(ipttt_ctx* ctx, const void* V, const void* Z, const void* W0, const float* W_init, int64_t B,
+                      int64_t T, int64_t d, int64_t f, int64_t C, ipttt_dtype dt, void* Wst, uint32_t* ctr, void* O,
+                      float* W_final, bool write_first, int call, bool* fuse) {
+  ipttt_status s = IPTTT_OK;
+  const bool bf16 = dt == IPTTT_BF16;
+  if (*fuse) {
+    s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr, W_init, write_first);
+    if (s == IPTTT_ERR_UNSUPPORTED) {
+      *fuse = false;  // the cooperative launch was refused: separate kernels below
+    } else if (s != IPTTT_OK) {
+      return s;
+    } else {
+      mark(ctx, call, kEvStateEnd, ctx->stream);
+      mark(ctx, call, kEvApplyEnd, ctx->stream);
+      if (call >= 0) ctx->timed_fused[call] = 1;
+      return IPTTT_OK;
+    }
+  }
+  const bool skip_first = bf16 && !write_first;
+  if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, skip_first, W_init)) != IPTTT_OK) return s;
+  mark(ctx, call, kEvStateEnd, ctx->stream);
+  const void* w0_first = (skip_first && W_init == nullptr) ? W0 : nullptr;
+  if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, w0_first)) != IPTTT_OK) return s;
+  mark(ctx, call, kEvApplyEnd, ctx->stream);
+  return IPTTT_OK;
+}
+
+// Step 1 of the pages' three-step scheme for one range of tokens (a rank of context
+// parallelism): Z and V of the range (the conv continuing from halo_in) into sv, and each
+// sequence's update total S[b] = sum_i V_i^T Z_i (V eta-scaled), accumulated from zero with no
+// per-chunk weight written.
+ipttt_status run_totals(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu, const void* Wt,
+                        const void* cw, const void* halo_in, int64_t B, int64_t T, int64_t d, int64_t f, int64_t C,
+                        int k, float eta, ipttt_dtype dt, float* S, const SavedPtrs& sv) {
+  ipttt_status s = IPTTT_OK;
+  if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  if ((s = run_swiglu(ctx, H, Wg, Wu, B * T, d, f, dt, sv.z)) != IPTTT_OK) return s;
+  if (Wt != nullptr) {
+    if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, sv.y, halo_in)) != IPTTT_OK) return s;
+    if ((s = run_target_gemm(ctx, sv.y, Wt, B * T, d, eta, dt, sv.v)) != IPTTT_OK) return s;
+  } else if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, sv.v, halo_in, eta)) != IPTTT_OK) {
+    return s;
+  }
+  if (dt != IPTTT_BF16)  // fp32: the delta stack and the scan from zero (the stack is scratch)
+    return run_state(ctx, sv.v, sv.z, nullptr, B, T, d, f, C, dt, sv.wst, S, false, nullptr);
+  const int64_t n = n_chunks_of(T, C);
+  CUtensorMap mv, mz, mf;
+  if (!map_3d(ctx, &mv, sv.v, B, T, d, 64) || !map_3d(ctx, &mz, sv.z, B, T, f, 64) ||
+      !map_3d_f32(ctx, &mf, S, B, d, f, 32))
+    return IPTTT_ERR_CUDA;
+  state::Params p{};
+  p.B = (int)B;
+  p.T = (int)T;
+  p.d = (int)d;
+  p.f = (int)f;
+  p.C = (int)C;
+  p.n_chunks = (int)n;
+  p.m_units = ceil_div(d, state::BMD);
+  p.n_units = ceil_div(f, state::BNF);
+  p.units = (int)(B * p.m_units * p.n_units);
+  p.skip_first = 1;
+  p.no_snap = 1;  // zero start (W0 and W_init NULL), only the final state is stored
+  p.st = dev_status(ctx);
+  return launch_state_kernel(ctx, mv, mz, mv, mf, p);
+}
+
 // The layer on device buffers, validated by the caller.
 // W_init (optional, fp32 [B, d, f]): per-sequence starting state instead of W0; halo_in /
 // halo_out (optional, [B, k-1, d]): the X0 rows before this call / after it (resumed calls).
@@ -101,26 +171,9 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
     if (ez != cudaSuccess) return cuda_fail(ctx, ez, "counter reset");
   }
   mark(ctx, call, kEvTargetEnd, ctx->stream);
-  if (fuse) {
-    s = run_state_apply_fused(ctx, V, Z, W0, B, T, d, f, C, Wst, W_final, O, ctr, W_init, sv != nullptr);
-    if (s == IPTTT_ERR_UNSUPPORTED) {
-      fuse = false;  // the cooperative launch was refused: separate kernels below
-    } else if (s != IPTTT_OK) {
-      return s;
-    } else {
-      mark(ctx, call, kEvStateEnd, ctx->stream);
-      mark(ctx, call, kEvApplyEnd, ctx->stream);
-      if (call >= 0) ctx->timed_fused[call] = 1;
-    }
-  }
-  if (!fuse) {
-    const bool skip_first = bf16 && sv == nullptr;  // the training forward keeps W_0 in the stack too
-    if ((s = run_state(ctx, V, Z, W0, B, T, d, f, C, dt, Wst, W_final, skip_first, W_init)) != IPTTT_OK) return s;
-    mark(ctx, call, kEvStateEnd, ctx->stream);
-    const void* w0_first = (skip_first && W_init == nullptr) ? W0 : nullptr;
-    if ((s = run_apply(ctx, Z, Wst, B, T, d, f, C, dt, O, w0_first)) != IPTTT_OK) return s;
-    mark(ctx, call, kEvApplyEnd, ctx->stream);
-  }
+  if ((s = run_tail(ctx, V, Z, W0, W_init, B, T, d, f, C, dt, Wst, ctr, O, W_final, sv != nullptr, call, &fuse)) !=
+      IPTTT_OK)
+    return s;
   if (call >= 0)
     ctx->timed_launches += (bf16 ? (fuse ? 4 : 5) : 6) + ((halo_out != nullptr && k > 1) ? 1 : 0) - (Wt ? 0 : 1);
   return IPTTT_OK;

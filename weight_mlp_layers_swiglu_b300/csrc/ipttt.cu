@@ -395,6 +395,119 @@ ipttt_status ipttt_layer_backward_saved(ipttt_ctx* ctx, const void* H, const voi
                            dX0, dW_gate, dW_up, dW_down0, dW_target, dconv_w, saved_ptrs(saved, SL), ws);
 }
 
+ipttt_status ipttt_layer_totals(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate, const void* W_up,
+                                const void* W_target, const void* conv_w, const void* X0_halo, int64_t B, int64_t T,
+                                int64_t d, int64_t d_ff, int64_t C, int k, float eta, ipttt_dtype dt, float* S,
+                                void* saved, size_t saved_bytes) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  const SavedLayout SL = saved_layout(B, T, d, d_ff, C, dt);
+  ipttt_status s = check_shape(ctx, B, T, d, d_ff, C, k, dt);
+  if (s != IPTTT_OK) return s;
+  if (!std::isfinite(eta)) {
+    set_err(ctx, "eta is not finite");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (B == 0) return IPTTT_OK;
+  const bool work = T > 0;
+  struct P {
+    const void* p;
+    const char* n;
+    bool needed;
+  } ptrs[] = {{H, "H", work},           {X0, "X0", work},       {W_gate, "W_gate", work}, {W_up, "W_up", work},
+              {conv_w, "conv_w", work}, {saved, "saved", work}, {S, "S", true},           {W_target, "W_target", false},
+              {X0_halo, "X0_halo", false}};
+  for (const P& q : ptrs) {
+    if (q.needed && !q.p) {
+      set_err(ctx, "%s is NULL", q.n);
+      return IPTTT_ERR_INVALID_ARG;
+    }
+    if (q.p && !aligned16(q.p)) {
+      set_err(ctx, "%s is not 16-byte aligned", q.n);
+      return IPTTT_ERR_INVALID_ARG;
+    }
+  }
+  if (work && saved_bytes < SL.total) {
+    set_err(ctx, "saved-activation buffer too small: %zu < %zu bytes", saved_bytes, SL.total);
+    return IPTTT_ERR_WORKSPACE;
+  }
+  const size_t es = esize(dt);
+  const size_t act = (size_t)B * T * d * es, wdf = (size_t)d * d_ff * es;
+  std::vector<Region> all = {{H, act, "H"},
+                             {X0, act, "X0"},
+                             {W_gate, wdf, "W_gate"},
+                             {W_up, wdf, "W_up"},
+                             {W_target, (size_t)d * d * es, "W_target"},
+                             {conv_w, (size_t)d * k * es, "conv_w"},
+                             {X0_halo, (size_t)B * (k - 1) * d * es, "X0_halo"},
+                             {S, (size_t)B * d * d_ff * 4, "S"},
+                             {saved, T > 0 ? SL.total : 0, "saved"}};
+  std::vector<Region> outs = {all[7], all[8]};
+  std::string what;
+  if (find_overlap(outs, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  if (T == 0) {
+    const cudaError_t e = cudaMemsetAsync(S, 0, (size_t)B * d * d_ff * 4, ctx->stream);
+    return e == cudaSuccess ? IPTTT_OK : cuda_fail(ctx, e, "total clear");
+  }
+  return run_totals(ctx, H, X0, W_gate, W_up, W_target, conv_w, X0_halo, B, T, d, d_ff, C, k, eta, dt, S,
+                    saved_ptrs(saved, SL));
+}
+
+ipttt_status ipttt_layer_apply_saved(ipttt_ctx* ctx, const float* W_init, int64_t B, int64_t T, int64_t d,
+                                     int64_t d_ff, int64_t C, ipttt_dtype dt, void* saved, size_t saved_bytes,
+                                     void* O, float* W_final) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, B, T, d, d_ff, C, 1, dt);
+  if (s != IPTTT_OK) return s;
+  if (B == 0) return IPTTT_OK;
+  const SavedLayout SL = saved_layout(B, T, d, d_ff, C, dt);
+  const bool work = T > 0;
+  if (!W_init || !W_final || !aligned16(W_init) || !aligned16(W_final) ||
+      (work && (!saved || !O || !aligned16(saved) || !aligned16(O)))) {
+    set_err(ctx, "apply_saved: NULL or misaligned pointer");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (work && saved_bytes < SL.total) {
+    set_err(ctx, "saved-activation buffer too small: %zu < %zu bytes", saved_bytes, SL.total);
+    return IPTTT_ERR_WORKSPACE;
+  }
+  const size_t state = (size_t)B * d * d_ff * 4;
+  std::vector<Region> all = {{saved, work ? SL.total : 0, "saved"}, {O, work ? (size_t)B * T * d * esize(dt) : 0, "O"},
+                             {W_init, state, "W_init"}};
+  std::vector<Region> outs = {all[1]};
+  std::string what;
+  if (find_overlap(outs, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  // W_final may be W_init itself (each state element is read before it is rewritten)
+  all.pop_back();
+  std::vector<Region> st_out = {{W_final, state, "W_final"}};
+  if (W_final != W_init) all.push_back({W_init, state, "W_init"});
+  if (find_overlap(st_out, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  cudaError_t e;
+  if (!work) {
+    if (W_final == W_init) return IPTTT_OK;
+    e = cudaMemcpyAsync(W_final, W_init, state, cudaMemcpyDeviceToDevice, ctx->stream);
+    return e == cudaSuccess ? IPTTT_OK : cuda_fail(ctx, e, "state copy");
+  }
+  const bool bf16 = dt == IPTTT_BF16;
+  if (bf16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  const SavedPtrs sv = saved_ptrs(saved, SL);
+  bool fuse = bf16 && ctx->fused_tail && ctx->coop;
+  if (fuse && (e = cudaMemsetAsync(sv.ctr, 0, (size_t)(B * n_chunks_of(T, C) + 1) * 4, ctx->stream)) != cudaSuccess)
+    return cuda_fail(ctx, e, "counter reset");
+  return run_tail(ctx, sv.v, sv.z, nullptr, W_init, B, T, d, d_ff, C, dt, sv.wst, sv.ctr, O, W_final, false, -1,
+                  &fuse);
+}
+
 ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
                                         const void* W_up, const void* W_target, const void* conv_w,
                                         const float* W_state, const void* X0_halo, int64_t B, int64_t T, int64_t d,

@@ -49,6 +49,7 @@ struct Params {
   int skip_first;               // 1: W_eff[b, 0] (= W_down0) is not written (the apply reads W_down0)
   const float* W_init;          // optional [B, d, f] fp32: each sequence's own starting state
   int reverse;                  // 1: chunks run last to first (the backward pass's suffix scan)
+  int no_snap;                  // 1: no W_eff snapshot at all, only the final state (update totals)
   DevStatus st;
 };
 
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_st32(t_row + c * 32, r);
         }
         tmem_st_wait();
-        if (!p.skip_first)
+        if (!p.skip_first && !p.no_snap)
           snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks + chunk_at(p, 0));
         tc_fence_before();
         mbar_arrive(&snap_done[slot]);
@@ -309,7 +310,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           decode_unit(p, u, b, mb, nb);
           const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BNF);
           if (i < p.n_chunks) {
-            snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks + chunk_at(p, i));
+            if (!p.no_snap)
+              snapshot_bf16(out, t_row, &map_weff, nb * BNF, mb * BMD + q * 32, b * p.n_chunks + chunk_at(p, i));
             tc_fence_before();
             mbar_arrive(&snap_done[slot]);
           } else {

@@ -207,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           tmem_st32(t_row + c * 32, r);
         }
         tmem_st_wait();
-        if (!p.skip_first)
+        if (!p.skip_first && !p.no_snap)
           state::snapshot_bf16(out, t_row, &map_weff, nb * BNF, row0 + q * 32, b * p.n_chunks + state::chunk_at(p, 0));
         release(slot);
       }
@@ -226,8 +226,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const int row0 = mb * PAIR_D + (int)rank * BMD;
           const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BNF);
           if (i < p.n_chunks) {
-            state::snapshot_bf16(out, t_row, &map_weff, nb * BNF, row0 + q * 32,
-                                 b * p.n_chunks + state::chunk_at(p, i));
+            if (!p.no_snap)
+              state::snapshot_bf16(out, t_row, &map_weff, nb * BNF, row0 + q * 32,
+                                   b * p.n_chunks + state::chunk_at(p, i));
             release(slot);
           } else {
             state::snapshot_f32(out, t_row, &map_wfin, nb * BNF, row0 + q * 32, b);

@@ -61,6 +61,10 @@ _SIGNATURES = {
                                                                              c_vp, ctypes.c_size_t] + [c_vp] * 10
                                    + [ctypes.c_size_t]),
     "ipttt_state_weight": (ctypes.c_int, [c_vp, c_vp] + [c_i64] * 3 + [ctypes.c_int, c_vp]),
+    "ipttt_layer_totals": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                                                     c_vp, c_vp, ctypes.c_size_t]),
+    "ipttt_layer_apply_saved": (ctypes.c_int, [c_vp, c_vp] + [c_i64] * 5 + [ctypes.c_int, c_vp, ctypes.c_size_t, c_vp,
+                                                                             c_vp]),
     "ipttt_swiglu": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, c_vp]),
     "ipttt_target": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_int, c_vp, c_vp]),
     "ipttt_chunk_state": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 5 + [ctypes.c_int, c_vp, c_vp]),
@@ -347,6 +351,44 @@ class Context:
                 "W_down0": torch.empty((d, f), **f32),
                 "W_target": torch.empty((d, d), **f32) if with_target else None,
                 "conv_w": torch.empty((d, k), **f32)}
+
+    def layer_totals(self, H, X0, W_gate, W_up, W_target, conv_w, X0_halo, C: int, eta: float, saved=None, S=None):
+        """Step 1 of the three-step scheme on a range of tokens: (S, saved), S [B,d,d_ff] fp32 the
+        range's update total (from zero), saved holding the range's Z and V for layer_apply_saved."""
+        B, T, d = H.shape
+        f = W_gate.shape[0]
+        k = conv_w.shape[1]
+        dt, dev = H.dtype, self.device
+        for t, n, s in ((H, "H", (B, T, d)), (X0, "X0", (B, T, d)), (W_gate, "W_gate", (f, d)),
+                        (W_up, "W_up", (f, d)), (conv_w, "conv_w", (d, k))):
+            _need(t, n, s, dt, dev)
+        if W_target is not None:
+            _need(W_target, "W_target", (d, d), dt, dev)
+        if X0_halo is not None:
+            _need(X0_halo, "X0_halo", (B, k - 1, d), dt, dev)
+        code = dtype_code(dt)
+        S = S if S is not None else torch.empty((B, d, f), dtype=torch.float32, device=dev)
+        if saved is None:
+            saved = torch.empty(max(saved_size(B, T, d, f, C, k, code), 256), dtype=torch.uint8, device=dev)
+        st = self.lib.ipttt_layer_totals(self.h, _ptr(H), _ptr(X0), _ptr(W_gate), _ptr(W_up), _ptr(W_target),
+                                         _ptr(conv_w), _ptr(X0_halo if X0_halo is None or X0_halo.numel() else None),
+                                         B, T, d, f, C, k, float(eta), code, _ptr(S), _ptr(saved),
+                                         saved.numel() * saved.element_size())
+        self._check(st, "layer_totals")
+        return S, saved
+
+    def layer_apply_saved(self, W_init, T: int, C: int, saved, dtype, O=None, W_final=None):
+        """Step 3 on the range whose Z and V layer_totals saved: (O [B,T,d], W_final [B,d,d_ff] fp32)
+        from each sequence's starting state W_init [B,d,d_ff] fp32."""
+        B, d, f = W_init.shape
+        dev = self.device
+        _need(W_init, "W_init", (B, d, f), torch.float32, dev)
+        O = O if O is not None else torch.empty((B, T, d), dtype=dtype, device=dev)
+        W_final = W_final if W_final is not None else torch.empty((B, d, f), dtype=torch.float32, device=dev)
+        st = self.lib.ipttt_layer_apply_saved(self.h, _ptr(W_init), B, T, d, f, C, dtype_code(dtype), _ptr(saved),
+                                              saved.numel() * saved.element_size(), _ptr(O), _ptr(W_final))
+        self._check(st, "layer_apply_saved")
+        return O, W_final
 
     def layer_resume(self, H, X0, W_gate, W_up, W_target, conv_w, W_state, X0_halo, C: int, eta: float,
                      O=None, W_state_out=None, X0_halo_out=None, workspace=None):
