@@ -87,6 +87,13 @@ __device__ __forceinline__ bool tile_active(const Params& p, int prob, int mt) {
   return true;
 }
 
+// The logistic function and SiLU of the bf16 epilogues.  The exponential goes through __expf and
+// the quotient through __fdividef (within 2 ulp; it gives 0 once the denominator passes 2^126,
+// the functions' limit there); each result is rounded to bf16, 8 significant bits, right after.
+// The IEEE-rounded quotient would cost the epilogue warps several times the instructions.
+__device__ __forceinline__ float sigmoid_bf16ep(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
+__device__ __forceinline__ float silu_bf16ep(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+
 // The SwiGLU adjoint for 64 columns n0.. of one token's row: dZ (fp32) in lo/hi, A and U read
 // from au_row = [A | U] (bf16, au_f columns each) and overwritten with dA and dU:
 // dA = dZ U s (1 + A (1 - s)), dU = dZ A s, s = sigmoid(A).  d_ff % 8 == 0, so each group of 8
@@ -115,7 +122,7 @@ __device__ __forceinline__ void swiglu_adjoint_row64(const uint32_t (&lo)[32], c
       const float z1 = __uint_as_float(v < 4 ? lo[j + 1] : hi[j + 1]);
       const float A0 = bf16_lo(aw[e]), A1 = bf16_hi(aw[e]);
       const float U0 = bf16_lo(uw[e]), U1 = bf16_hi(uw[e]);
-      const float s0 = 1.0f / (1.0f + __expf(-A0)), s1 = 1.0f / (1.0f + __expf(-A1));
+      const float s0 = sigmoid_bf16ep(A0), s1 = sigmoid_bf16ep(A1);
       daw[e] = pack_bf16x2(z0 * U0 * s0 * (1.0f + A0 * (1.0f - s0)), z1 * U1 * s1 * (1.0f + A1 * (1.0f - s1)));
       duw[e] = pack_bf16x2(z0 * A0 * s0, z1 * A1 * s1);
     }
@@ -302,8 +309,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float a0 = __uint_as_float(g[2 * e]), a1 = __uint_as_float(g[2 * e + 1]);
-              const float z0 = a0 / (1.0f + __expf(-a0)) * __uint_as_float(u[2 * e]);
-              const float z1 = a1 / (1.0f + __expf(-a1)) * __uint_as_float(u[2 * e + 1]);
+              const float z0 = silu_bf16ep(a0) * __uint_as_float(u[2 * e]);
+              const float z1 = silu_bf16ep(a1) * __uint_as_float(u[2 * e + 1]);
               row[c * 16 + e] = pack_bf16x2(z0, z1);
             }
           }
