@@ -224,6 +224,25 @@ ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const 
 ipttt_status ipttt_state_weight(ipttt_ctx* ctx, const float* W_state, int64_t B, int64_t d, int64_t d_ff,
                                 ipttt_dtype dtype, void* W);
 
+/* One decode step of a stream (§3.2 Step 3 for the tokens of a chunk that is not complete yet):
+ * for m (1..8) new tokens of each of B sequences, Z = SiLU(H W_gate^T) * (H W_up^T) and
+ * O[b] = Z[b] W_cur[b]^T, W_cur [B, d, d_ff] dtype being each sequence's weight at the
+ * chunk's start (ipttt_state_weight of its state).  H [B, m, d] in; Z [B, m, d_ff] and
+ * O [B, m, d] out, all dtype, all device.  With the chunk buffers H_buf and X0_buf
+ * ([B, C, d], both or neither), the step also stores H[b, t] and X0[b, t] (X0 [B, m, d]) at
+ * token pos + t of the buffers (pos + m <= C), so that the chunk's update can be committed
+ * with ipttt_layer_forward_resume once it completes.  The apply, and the SwiGLU of a single
+ * token row (or of any rows in fp32), run on the CUDA cores as weight-streaming dot products
+ * over every SM with fp32 sums in a fixed order (the same on every run); several bf16 rows take
+ * the tensor-core SwiGLU.  The outputs agree with the chunked path's to rounding, not bit for
+ * bit.
+ * Outputs must not overlap inputs or each other.  Errors: INVALID_ARG, UNSUPPORTED (m outside
+ * 1..8; as ipttt_workspace_size for d, d_ff, dtype), CUDA. */
+ipttt_status ipttt_decode_step(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
+                               const void* W_up, const void* W_cur, int64_t B, int64_t m, int64_t d,
+                               int64_t d_ff, ipttt_dtype dtype, void* Z, void* O, void* H_buf,
+                               void* X0_buf, int64_t C, int64_t pos);
+
 /* ---- backward pass ----
  * The pages train the layer (§5 results: continued training of a 4B model, experiment 1, and
  * pretraining from scratch, experiment 3) but print no gradient formulas; these are the exact

@@ -402,4 +402,63 @@ ipttt_status run_state_apply_fused(ipttt_ctx* ctx, const void* V, const void* Z,
   return check_launch(ctx, "state+apply launch");
 }
 
+// A decode step's rows (simt.cuh, decode rows).  The SwiGLU of one token row streams the
+// weights on the CUDA cores (2 columns per block, 2 slices per warp in flight); several bf16
+// rows go through the tensor-core SwiGLU GEMM, which streams them as fast whatever the row
+// count up to a tile (the fp32 path has no tensor-core GEMM: its rows stay on the CUDA cores,
+// in launches of up to DEC_ROWS rows).  The first SwiGLU launch fills the chunk buffers, or two
+// strided copies do.  Then each sequence's m rows are applied with its weight W_cur[b] on the
+// CUDA cores (one row: 2 weight rows per block; more: 8 weight rows per block).
+template <typename E>
+ipttt_status run_decode_rows(ipttt_ctx* ctx, const void* H, const void* X0, const void* Wg, const void* Wu,
+                             const void* Wc, int64_t B, int64_t m, int64_t d, int64_t f, int64_t C, int64_t pos,
+                             void* Z, void* O, void* H_buf, void* X0_buf) {
+  constexpr int R = simt::DEC_ROWS;
+  constexpr bool kF32 = std::is_same<E, float>::value;
+  const E* h = static_cast<const E*>(H);
+  E* z = static_cast<E*>(Z);
+  const int64_t rows = B * m;
+  const int64_t cap = (int64_t)ctx->sm_count * 8;
+  auto grid = [&](int64_t groups) { return (unsigned)(groups < cap ? groups : cap); };
+  ipttt_status s = IPTTT_OK;
+  if (kF32 || rows == 1) {
+    for (int64_t r0 = 0; r0 < rows; r0 += R) {
+      const int nr = (int)(rows - r0 < R ? rows - r0 : R);
+      const bool copy = r0 == 0 && H_buf != nullptr;
+      const E* hc = copy ? h : nullptr;
+      const E* xc = copy ? static_cast<const E*>(X0) : nullptr;
+      E* hb = copy ? static_cast<E*>(H_buf) : nullptr;
+      E* xb = copy ? static_cast<E*>(X0_buf) : nullptr;
+      if (nr == 1)
+        simt::decode_swiglu_kernel<E, 1, 2, 2><<<grid(ceil_div(f, 2)), simt::DEC_THREADS, 0, ctx->stream>>>(
+            h + r0 * d, static_cast<const E*>(Wg), static_cast<const E*>(Wu), z + r0 * f, nr, (int)d, (int)f, hc, xc,
+            hb, xb, (int)B, (int)m, C, pos);
+      else
+        simt::decode_swiglu_kernel<E, R, 2, 1><<<grid(ceil_div(f, 2)), simt::DEC_THREADS, 0, ctx->stream>>>(
+            h + r0 * d, static_cast<const E*>(Wg), static_cast<const E*>(Wu), z + r0 * f, nr, (int)d, (int)f, hc, xc,
+            hb, xb, (int)B, (int)m, C, pos);
+      if ((s = check_launch(ctx, "decode SwiGLU launch")) != IPTTT_OK) return s;
+    }
+  } else {
+    if (H_buf != nullptr) {  // [B, m, d] -> rows pos.. of [B, C, d]
+      const size_t w = (size_t)(m * d) * sizeof(E), dp = (size_t)(C * d) * sizeof(E), off = (size_t)(pos * d);
+      cudaError_t e;
+      if ((e = cudaMemcpy2DAsync(static_cast<E*>(H_buf) + off, dp, H, w, w, (size_t)B, cudaMemcpyDeviceToDevice,
+                                 ctx->stream)) != cudaSuccess ||
+          (e = cudaMemcpy2DAsync(static_cast<E*>(X0_buf) + off, dp, X0, w, w, (size_t)B, cudaMemcpyDeviceToDevice,
+                                 ctx->stream)) != cudaSuccess)
+        return cuda_fail(ctx, e, "decode chunk buffers");
+    }
+    if ((s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+    if ((s = run_swiglu(ctx, H, Wg, Wu, rows, d, f, IPTTT_BF16, Z)) != IPTTT_OK) return s;
+  }
+  if (m == 1)
+    simt::decode_apply_kernel<E, 1, 2, 2><<<grid(B * d / 2), simt::DEC_THREADS, 0, ctx->stream>>>(
+        z, static_cast<const E*>(Wc), static_cast<E*>(O), (int)B, (int)m, (int)d, (int)f);
+  else
+    simt::decode_apply_kernel<E, R, 8, 1><<<grid(B * d / 8), simt::DEC_THREADS, 0, ctx->stream>>>(
+        z, static_cast<const E*>(Wc), static_cast<E*>(O), (int)B, (int)m, (int)d, (int)f);
+  return check_launch(ctx, "decode apply launch");
+}
+
 }  // namespace

@@ -750,6 +750,59 @@ ipttt_status ipttt_state_weight(ipttt_ctx* ctx, const float* W_state, int64_t B,
   return check_launch(ctx, "state weight launch");
 }
 
+ipttt_status ipttt_decode_step(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate, const void* W_up,
+                               const void* W_cur, int64_t B, int64_t m, int64_t d, int64_t d_ff, ipttt_dtype dt,
+                               void* Z, void* O, void* H_buf, void* X0_buf, int64_t C, int64_t pos) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, B, m, d, d_ff, 1, 1, dt, false);
+  if (s != IPTTT_OK) return s;
+  if (m < 1 || m > simt::DEC_ROWS) {
+    set_err(ctx, "decode step takes 1..%d tokens per sequence (m=%lld)", simt::DEC_ROWS, (long long)m);
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  if (B == 0) return IPTTT_OK;
+  const void* need[] = {H, W_gate, W_up, W_cur, Z, O};
+  for (const void* q : need) {
+    if (!q || !aligned16(q)) {
+      set_err(ctx, "decode step: NULL or misaligned pointer");
+      return IPTTT_ERR_INVALID_ARG;
+    }
+  }
+  const bool buf = H_buf != nullptr || X0_buf != nullptr;
+  if (buf) {
+    if (!H_buf || !X0_buf || !X0 || !aligned16(H_buf) || !aligned16(X0_buf) || !aligned16(X0)) {
+      set_err(ctx, "decode step: the chunk buffers need H_buf, X0_buf and X0, 16-byte aligned");
+      return IPTTT_ERR_INVALID_ARG;
+    }
+    if (C < 1 || pos < 0 || pos + m > C || B * C > (int64_t(1) << 31)) {
+      set_err(ctx, "decode step: tokens %lld..%lld do not fit a chunk buffer of %lld", (long long)pos,
+              (long long)(pos + m), (long long)C);
+      return IPTTT_ERR_INVALID_ARG;
+    }
+  }
+  const size_t es = esize(dt);
+  const size_t act = (size_t)(B * m * d) * es, wdf = (size_t)(d * d_ff) * es, bufb = buf ? (size_t)(B * C * d) * es : 0;
+  std::vector<Region> all = {{H, act, "H"},
+                             {buf ? X0 : nullptr, buf ? act : 0, "X0"},
+                             {W_gate, wdf, "W_gate"},
+                             {W_up, wdf, "W_up"},
+                             {W_cur, (size_t)B * wdf, "W_cur"},
+                             {Z, (size_t)(B * m * d_ff) * es, "Z"},
+                             {O, act, "O"},
+                             {H_buf, bufb, "H_buf"},
+                             {X0_buf, bufb, "X0_buf"}};
+  std::vector<Region> outs = {all[5], all[6], all[7], all[8]};
+  std::string what;
+  if (find_overlap(outs, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  if (dt == IPTTT_BF16)
+    return run_decode_rows<__nv_bfloat16>(ctx, H, X0, W_gate, W_up, W_cur, B, m, d, d_ff, C, pos, Z, O, H_buf, X0_buf);
+  return run_decode_rows<float>(ctx, H, X0, W_gate, W_up, W_cur, B, m, d, d_ff, C, pos, Z, O, H_buf, X0_buf);
+}
+
 ipttt_status ipttt_timing_begin(ipttt_ctx* ctx) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
   ctx->timing = true;

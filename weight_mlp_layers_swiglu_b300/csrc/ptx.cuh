@@ -433,4 +433,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// The logistic function and SiLU wherever the result is rounded to bf16 (8 significant bits)
+// right after.  The exponential goes through __expf and the quotient through __fdividef
+// (within 2 ulp; it gives 0 once the denominator passes 2^126, the functions' limit there).
+// The IEEE-rounded quotient would cost the tensor-core epilogue warps several times the
+// instructions.  The fp32 path keeps expf and the IEEE quotient.
+__device__ __forceinline__ float sigmoid_bf16ep(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
+__device__ __forceinline__ float silu_bf16ep(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+
 }  // namespace ipttt

@@ -430,6 +430,224 @@ __global__ void state_weight_kernel(const float* __restrict__ state, T* __restri
   if (e < n) W[e] = static_cast<T>(state[e]);
 }
 
+// --------------------------------------------------------------------------- decode rows
+// The few token rows of a decode step (zhichai.net page, §3.2 Step 3: the tokens of a chunk
+// that is not complete yet see the weight at the chunk's start).  For a handful of rows these
+// products stream each weight once at about one FLOP per byte, so they run on the CUDA cores
+// across every SM: one warp per output column, each lane summing its 8-element slices in k
+// order in fp32, then a fixed butterfly across the warp (the same result on every run).  The
+// weights are read with the streaming cache hint; the few rows they meet stay in L1.
+constexpr int DEC_ROWS = 8;  // rows of one SwiGLU launch; tokens per sequence of the apply
+constexpr int DEC_THREADS = 256;
+
+// Eight weight elements as loaded (streaming cache hint), widened to fp32 when used.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = __ldcs(reinterpret_cast<const float4*>(p));
+    b = __ldcs(reinterpret_cast<const float4*>(p + 4));
+  }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 w;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { w = __ldcs(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+  }
+};
+
+// SiLU as each path computes it: the IEEE quotient in fp32, the fast one before a bf16 rounding.
+template <typename T>
+__device__ __forceinline__ float silu_of(float a);
+template <>
+__device__ __forceinline__ float silu_of<float>(float a) { return a / (1.0f + expf(-a)); }
+template <>
+__device__ __forceinline__ float silu_of<__nv_bfloat16>(float a) { return silu_bf16ep(a); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Z[r, n] = SiLU(H[r] . W_gate[n]) * (H[r] . W_up[n]) for the R <= RMAX rows of H [R, d].
+// A block takes NB columns n at a time; its 8 warps split each dot product over interleaved
+// 256-element slices of d (warp w: slices w, w+8, ...), with NB*NBATCH slices' weight loads in
+// flight per lane, and the warps' partial sums meet in shared memory in warp order.
+// The first launch of a step may also copy the step's tokens into the chunk buffers:
+// H_buf[b, pos + t] = Hc[b, t] and X0_buf[b, pos + t] = X0c[b, t] for b < Bc, t < mc
+// ([Bc, mc, d] in, [Bc, C, d] buffers; H_buf NULL: no copy).
+template <typename T, int RMAX, int NB, int NBATCH>
+__global__ void __launch_bounds__(DEC_THREADS) decode_swiglu_kernel(const T* __restrict__ H, const T* __restrict__ Wg,
+                                                                    const T* __restrict__ Wu, T* __restrict__ Z, int R,
+                                                                    int d, int f, const T* __restrict__ Hc,
+                                                                    const T* __restrict__ X0c, T* __restrict__ H_buf,
+                                                                    T* __restrict__ X0_buf, int Bc, int mc, int64_t C,
+                                                                    int64_t pos) {
+  constexpr int NW = DEC_THREADS / 32;
+  __shared__ float part[NW][NB][RMAX][2];
+  if (H_buf != nullptr) {
+    const int64_t per_row = d / 8;
+    const int64_t nvec = (int64_t)Bc * mc * per_row;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
+      const int64_t row = v / per_row, c = (v - row * per_row) * 8;
+      const int64_t b = row / mc, t = row - b * mc;
+      const int64_t dst = (b * C + pos + t) * d + c;
+      float x[8];
+      load8(Hc + row * d + c, x);
+      store8(H_buf + dst, x);
+      load8(X0c + row * d + c, x);
+      store8(X0_buf + dst, x);
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int n0 = blockIdx.x * NB; n0 < f; n0 += gridDim.x * NB) {
+    float ag[NB][RMAX], au[NB][RMAX];
+#pragma unroll
+    for (int c = 0; c < NB; ++c)
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) ag[c][r] = au[c][r] = 0.f;
+    for (int k0 = (warp * 32 + lane) * 8; k0 < d; k0 += NW * 256 * NBATCH) {
+      Raw8<T> gw[NBATCH][NB], uw[NBATCH][NB];
+#pragma unroll
+      for (int j = 0; j < NBATCH; ++j)
+#pragma unroll
+        for (int c = 0; c < NB; ++c)
+          if (k0 + j * NW * 256 < d && n0 + c < f) {
+            gw[j][c].load(Wg + (int64_t)(n0 + c) * d + k0 + j * NW * 256);
+            uw[j][c].load(Wu + (int64_t)(n0 + c) * d + k0 + j * NW * 256);
+          }
+#pragma unroll
+      for (int j = 0; j < NBATCH; ++j) {
+        const int k = k0 + j * NW * 256;
+        if (k >= d) break;
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          if (r < R) {
+            float h[8];
+            load8(H + (int64_t)r * d + k, h);
+#pragma unroll
+            for (int c = 0; c < NB; ++c) {
+              if (n0 + c < f) {
+                float g[8], u[8];
+                gw[j][c].get(g);
+                uw[j][c].get(u);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  ag[c][r] = fmaf(g[e], h[e], ag[c][r]);
+                  au[c][r] = fmaf(u[e], h[e], au[c][r]);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < NB; ++c)
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r)
+        if (r < R) {
+          const float a = warp_sum(ag[c][r]), u = warp_sum(au[c][r]);
+          if (lane == 0) {
+            part[warp][c][r][0] = a;
+            part[warp][c][r][1] = u;
+          }
+        }
+    __syncthreads();
+    if ((int)threadIdx.x < NB * R) {
+      const int c = threadIdx.x / R, r = threadIdx.x - c * R;
+      if (n0 + c < f) {
+        float a = 0.f, u = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          a += part[w][c][r][0];
+          u += part[w][c][r][1];
+        }
+        Z[(int64_t)r * f + n0 + c] = static_cast<T>(silu_of<T>(a) * u);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// O[b, t, e] = sum_n Z[b, t, n] * W[b, e, n] for the R <= RMAX rows t of each of the Bq
+// sequences: Z [Bq, R, f], W [Bq, d, f] (each sequence's current chunk weight), O [Bq, R, d].
+// A block takes NB rows e of one sequence at a time (d % NB == 0), split over its warps as in
+// decode_swiglu_kernel.
+template <typename T, int RMAX, int NB, int NBATCH>
+__global__ void __launch_bounds__(DEC_THREADS) decode_apply_kernel(const T* __restrict__ Z, const T* __restrict__ W,
+                                                                   T* __restrict__ O, int Bq, int R, int d, int f) {
+  constexpr int NW = DEC_THREADS / 32;
+  __shared__ float part[NW][NB][RMAX];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t groups = (int64_t)Bq * d / NB;
+  for (int64_t q = blockIdx.x; q < groups; q += gridDim.x) {
+    const int64_t row0 = q * NB;  // rows row0 .. row0+NB-1 of the [Bq*d, f] weight stack
+    const int64_t b = row0 / d;
+    const T* z = Z + b * R * f;
+    float acc[NB][RMAX];
+#pragma unroll
+    for (int c = 0; c < NB; ++c)
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) acc[c][r] = 0.f;
+    for (int n0 = (warp * 32 + lane) * 8; n0 < f; n0 += NW * 256 * NBATCH) {
+      Raw8<T> ww[NBATCH][NB];
+#pragma unroll
+      for (int j = 0; j < NBATCH; ++j)
+#pragma unroll
+        for (int c = 0; c < NB; ++c)
+          if (n0 + j * NW * 256 < f) ww[j][c].load(W + (row0 + c) * f + n0 + j * NW * 256);
+#pragma unroll
+      for (int j = 0; j < NBATCH; ++j) {
+        const int n = n0 + j * NW * 256;
+        if (n >= f) break;
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          if (r < R) {
+            float zv[8];
+            load8(z + (int64_t)r * f + n, zv);
+#pragma unroll
+            for (int c = 0; c < NB; ++c) {
+              float wv[8];
+              ww[j][c].get(wv);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[c][r] = fmaf(wv[i], zv[i], acc[c][r]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < NB; ++c)
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r)
+        if (r < R) {
+          const float o = warp_sum(acc[c][r]);
+          if (lane == 0) part[warp][c][r] = o;
+        }
+    __syncthreads();
+    if ((int)threadIdx.x < NB * R) {
+      const int c = threadIdx.x / R, r = threadIdx.x - c * R;
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) o += part[w][c][r];
+      const int64_t e = row0 + c - b * d;
+      O[(b * R + r) * d + e] = static_cast<T>(o);
+    }
+    __syncthreads();
+  }
+}
+
 // Device-side wait that nothing ever signals: exercises the bounded-wait path.
 __global__ void wait_probe_kernel(DevStatus st) {
   __shared__ __align__(8) uint64_t bar;

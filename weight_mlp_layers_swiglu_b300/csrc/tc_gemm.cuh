@@ -87,13 +87,6 @@ __device__ __forceinline__ bool tile_active(const Params& p, int prob, int mt) {
   return true;
 }
 
-// The logistic function and SiLU of the bf16 epilogues.  The exponential goes through __expf and
-// the quotient through __fdividef (within 2 ulp; it gives 0 once the denominator passes 2^126,
-// the functions' limit there); each result is rounded to bf16, 8 significant bits, right after.
-// The IEEE-rounded quotient would cost the epilogue warps several times the instructions.
-__device__ __forceinline__ float sigmoid_bf16ep(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
-__device__ __forceinline__ float silu_bf16ep(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
-
 // The SwiGLU adjoint for 64 columns n0.. of one token's row: dZ (fp32) in lo/hi, A and U read
 // from au_row = [A | U] (bf16, au_f columns each) and overwritten with dA and dU:
 // dA = dZ U s (1 + A (1 - s)), dU = dZ A s, s = sigmoid(A).  d_ff % 8 == 0, so each group of 8

@@ -243,8 +243,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float a0 = __uint_as_float(g[2 * e]), a1 = __uint_as_float(g[2 * e + 1]);
-              const float z0 = gemm::silu_bf16ep(a0) * __uint_as_float(u[2 * e]);
-              const float z1 = gemm::silu_bf16ep(a1) * __uint_as_float(u[2 * e + 1]);
+              const float z0 = silu_bf16ep(a0) * __uint_as_float(u[2 * e]);
+              const float z1 = silu_bf16ep(a1) * __uint_as_float(u[2 * e + 1]);
               row[c * 16 + e] = pack_bf16x2(z0, z1);
             }
           }

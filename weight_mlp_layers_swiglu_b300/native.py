@@ -61,6 +61,7 @@ _SIGNATURES = {
                                                                              c_vp, ctypes.c_size_t] + [c_vp] * 10
                                    + [ctypes.c_size_t]),
     "ipttt_state_weight": (ctypes.c_int, [c_vp, c_vp] + [c_i64] * 3 + [ctypes.c_int, c_vp]),
+    "ipttt_decode_step": (ctypes.c_int, [c_vp] * 6 + [c_i64] * 4 + [ctypes.c_int] + [c_vp] * 4 + [c_i64] * 2),
     "ipttt_layer_totals": (ctypes.c_int, [c_vp] * 8 + [c_i64] * 5 + [ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                                                      c_vp, c_vp, ctypes.c_size_t]),
     "ipttt_layer_apply_saved": (ctypes.c_int, [c_vp, c_vp] + [c_i64] * 5 + [ctypes.c_int, c_vp, ctypes.c_size_t, c_vp,
@@ -458,6 +459,30 @@ class Context:
                     "state_weight")
         return W
 
+    def decode_step(self, H, W_gate, W_up, W_cur, X0=None, H_buf=None, X0_buf=None, pos: int = 0, O=None, Z=None):
+        """A decode step (ipttt_decode_step): (O [B,m,d], Z [B,m,d_ff]) for m (1..8) new tokens H
+        [B,m,d] of each sequence, applied with each sequence's chunk weight W_cur [B,d,d_ff].  With
+        the chunk buffers H_buf and X0_buf [B,C,d], H and X0 [B,m,d] are also stored at tokens
+        pos.. of the buffers."""
+        B, m, d = H.shape
+        f = W_gate.shape[0]
+        dt, dev = H.dtype, self.device
+        _need(H, "H", (B, m, d), dt, dev)
+        for t, n, shp in ((W_gate, "W_gate", (f, d)), (W_up, "W_up", (f, d)), (W_cur, "W_cur", (B, d, f))):
+            _need(t, n, shp, dt, dev)
+        C = 0
+        if H_buf is not None or X0_buf is not None:
+            C = H_buf.shape[1]
+            _need(H_buf, "H_buf", (B, C, d), dt, dev)
+            _need(X0_buf, "X0_buf", (B, C, d), dt, dev)
+            _need(X0, "X0", (B, m, d), dt, dev)
+        O = O if O is not None else torch.empty((B, m, d), dtype=dt, device=dev)
+        Z = Z if Z is not None else torch.empty((B, m, f), dtype=dt, device=dev)
+        st = self.lib.ipttt_decode_step(self.h, _ptr(H), _ptr(X0), _ptr(W_gate), _ptr(W_up), _ptr(W_cur), B, m, d, f,
+                                        dtype_code(dt), _ptr(Z), _ptr(O), _ptr(H_buf), _ptr(X0_buf), C, pos)
+        self._check(st, "decode_step")
+        return O, Z
+
     # ------------------------------------------------------------------ the steps
     def swiglu(self, H2d, W_gate, W_up, Z=None):
         rows, d = H2d.shape
@@ -533,22 +558,30 @@ class Context:
         self._check(self.lib.ipttt_selftest_wait_timeout(self.h), "selftest_wait_timeout")
 
 
+DECODE_MAX_TOKENS = 8  # tokens per sequence that one ipttt_decode_step takes
+
+
 class StreamingLayer:
     """Keeps the per-sequence fast-weight state and conv halo of B sequences across calls.
 
     step() takes any number of tokens per call (one token at a time for decoding):
       * whole chunks starting at a chunk boundary run through the resumable layer;
       * tokens of a chunk that is not complete yet are applied at once with the weight at the
-        chunk's start (Z from the SwiGLU step, then the chunk apply with that weight), and their
-        inputs are buffered; when the chunk completes, its update is committed by running the
-        resumable layer over the buffered chunk (the C-token buffer of a decode loop).
-    Every output and the state after every complete chunk equal those of one call over the whole
-    sequence bit for bit.  flush() commits a final partial chunk, after which `state` is the
-    final W_down of the whole sequence.  Buffers only: all compute runs in the library.
+        chunk's start, and their inputs are buffered; when the chunk completes, its update is
+        committed by running the resumable layer over the buffered chunk (the C-token buffer of
+        a decode loop).  Up to 8 such tokens per call go through ipttt_decode_step (the CUDA-core
+        decode rows); more, or all of them with exact=True, through the SwiGLU step and the chunk
+        apply, the tensor-core kernels of the chunked call.
+    The state after every complete chunk equals that of one call over the whole sequence bit for
+    bit, and so do the outputs of whole chunks and, with exact=True, every output; the decode
+    rows agree with them to rounding.  flush() commits a final partial chunk, after which
+    `state` is the final W_down of the whole sequence.  Buffers only: all compute runs in the
+    library.
     """
 
-    def __init__(self, ctx: Context, W_gate, W_up, W_down0, W_target, conv_w, B: int, C: int, eta: float):
-        self.ctx, self.C, self.eta, self.B = ctx, C, eta, B
+    def __init__(self, ctx: Context, W_gate, W_up, W_down0, W_target, conv_w, B: int, C: int, eta: float,
+                 exact: bool = False):
+        self.ctx, self.C, self.eta, self.B, self.exact = ctx, C, eta, B, exact
         self.W_gate, self.W_up, self.W_target, self.conv_w = W_gate, W_up, W_target, conv_w
         d, f = W_down0.shape
         k = conv_w.shape[1]
@@ -593,10 +626,15 @@ class StreamingLayer:
                 self.ctx.state_weight(self.state, self.dtype, self.W_cur)
                 self._w_cur_ok = True
             h = H[:, pos:pos + m].contiguous()
-            Z = self.ctx.swiglu(h.view(B * m, d), self.W_gate, self.W_up)
-            outs.append(self.ctx.chunk_apply(Z.view(B, m, self.f), self.W_cur.view(B, 1, d, self.f), self.C))
-            self._pend_H[:, self.pending:self.pending + m] = h
-            self._pend_X[:, self.pending:self.pending + m] = X0[:, pos:pos + m]
+            if self.exact or m > DECODE_MAX_TOKENS:
+                Z = self.ctx.swiglu(h.view(B * m, d), self.W_gate, self.W_up)
+                outs.append(self.ctx.chunk_apply(Z.view(B, m, self.f), self.W_cur.view(B, 1, d, self.f), self.C))
+                self._pend_H[:, self.pending:self.pending + m] = h
+                self._pend_X[:, self.pending:self.pending + m] = X0[:, pos:pos + m]
+            else:
+                O_t, _ = self.ctx.decode_step(h, self.W_gate, self.W_up, self.W_cur, X0[:, pos:pos + m].contiguous(),
+                                              self._pend_H, self._pend_X, self.pending)
+                outs.append(O_t)
             self.pending += m
             pos += m
             if self.pending == self.C:
