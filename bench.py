@@ -367,8 +367,23 @@ def stream_leg(args, w, ctx, weights, H, X0, dev, world):
     ms_dec = max_over_ranks(ms_dec, world, dev)
     return {"call_tokens": S, "calls_per_sequence": len(cuts), "value": w.B * w.T * world / (ms * 1e-3),
             "unit": UNIT, "ms_per_sequence": ms,
-            "decode": {"tokens_per_call": 1, "tokens": n_dec, "value": w.B * n_dec * world / (ms_dec * 1e-3),
-                       "unit": UNIT, "ms_per_token": ms_dec / n_dec}}
+            "decode": decode_line(w, n_dec, ms_dec, world)}
+
+
+def decode_line(w, n_dec: int, ms_dec: float, world: int) -> dict:
+    """The decode sub-leg: one token per call for n_dec calls (one chunk, its commit included).
+    Each call streams W_gate, W_up and every sequence's chunk weight once; that traffic over the
+    measured time, against the measured HBM bandwidth, is the leg's roofline."""
+    es = 4 if w.dtype == "f32" else 2
+    step_bytes = (2 * w.d * w.d_ff + w.B * w.d * w.d_ff) * es
+    peaks, src = load_peaks()
+    gbs = step_bytes * n_dec / (ms_dec * 1e-3) / 1e9
+    return {"tokens_per_call": 1, "tokens": n_dec, "value": w.B * n_dec * world / (ms_dec * 1e-3), "unit": UNIT,
+            "ms_per_token": ms_dec / n_dec,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": step_bytes,
+                         "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else src,
+                         "note": "weights streamed once per one-token call; the chunk's commit is inside the time"}}
 
 
 def run_cp(args, w):
