@@ -83,3 +83,27 @@ def test_random_shape_resume(ctx, seed):
     assert rel_err(O, O_ref) <= TOL[dt], shape
     assert rel_err(Ws, W_ref) <= TOL[dt], shape
     assert torch.equal(h.cpu().double(), torch.from_numpy(h_ref)), shape
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shape_decode_step(ctx, seed):
+    """ipttt_decode_step on drawn shapes (1..8 tokens of 1..6 sequences, widths on and off the
+    tiles, both dtypes) against the oracle's SwiGLU and chunk apply."""
+    r = np.random.default_rng(9000 + seed)
+    dt = "bf16" if r.random() < 0.7 else "f32"
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    B = int(r.integers(1, 7))
+    m = int(r.integers(1, 9))
+    d = int(r.choice([8, 64, 136, 256, 520, 1032]))
+    f = int(r.choice([8, 128, 264, 776, 2056]))
+    H = seeded((B, m, d), 1.0, tdt, 9100 + seed)
+    Wg = seeded((f, d), d ** -0.5, tdt, 9200 + seed)
+    Wu = seeded((f, d), d ** -0.5, tdt, 9300 + seed)
+    Wc = seeded((B, d, f), f ** -0.5, tdt, 9400 + seed)
+    O, Z = ctx.decode_step(H.cuda(), Wg.cuda(), Wu.cuda(), Wc.cuda())
+    assert ctx.sync() == 0, ctx.last_error()
+    shape = (dt, B, m, d, f)
+    for b in range(B):
+        Z_ref = oracle.swiglu(H[b], Wg, Wu)
+        assert rel_err(Z[b], Z_ref) <= TOL[dt], (b, shape)
+        assert rel_err(O[b], oracle.chunk_apply(Z_ref, Wc[b][None], m)) <= TOL[dt], (b, shape)
