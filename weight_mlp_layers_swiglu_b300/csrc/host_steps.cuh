@@ -452,12 +452,31 @@ ipttt_status run_decode_rows(ipttt_ctx* ctx, const void* H, const void* X0, cons
     if ((s = ensure_attrs(ctx)) != IPTTT_OK) return s;
     if ((s = run_swiglu(ctx, H, Wg, Wu, rows, d, f, IPTTT_BF16, Z)) != IPTTT_OK) return s;
   }
-  if (m == 1)
-    simt::decode_apply_kernel<E, 1, 2, 2><<<grid(B * d / 2), simt::DEC_THREADS, 0, ctx->stream>>>(
-        z, static_cast<const E*>(Wc), static_cast<E*>(O), (int)B, (int)m, (int)d, (int)f);
-  else
-    simt::decode_apply_kernel<E, R, 8, 1><<<grid(B * d / 8), simt::DEC_THREADS, 0, ctx->stream>>>(
-        z, static_cast<const E*>(Wc), static_cast<E*>(O), (int)B, (int)m, (int)d, (int)f);
+  // the apply starts as a dependent launch: it prefetches W_cur into L2 while the SwiGLU rows
+  // stream theirs (when W_cur takes at most half the L2), then waits for Z
+  const int64_t wc_bytes = B * d * f * (int64_t)sizeof(E);
+  const int prefetch = wc_bytes <= (int64_t)64 << 20;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(simt::DEC_THREADS);
+  cfg.stream = ctx->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const E* wc = static_cast<const E*>(Wc);
+  E* o = static_cast<E*>(O);
+  cudaError_t e;
+  if (m == 1) {
+    cfg.gridDim = dim3(grid(B * d / 2));
+    e = cudaLaunchKernelEx(&cfg, simt::decode_apply_kernel<E, 1, 2, 2>, (const E*)z, wc, o, (int)B, (int)m, (int)d,
+                           (int)f, prefetch);
+  } else {
+    cfg.gridDim = dim3(grid(B * d / 8));
+    e = cudaLaunchKernelEx(&cfg, simt::decode_apply_kernel<E, R, 8, 1>, (const E*)z, wc, o, (int)B, (int)m, (int)d,
+                           (int)f, prefetch);
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "decode apply launch");
   return check_launch(ctx, "decode apply launch");
 }
 

@@ -423,6 +423,20 @@ struct OutStager {
   }
 };
 
+// ----------------------------------------------------------------- dependent launches
+// Programmatic dependent launch: a kernel lets the next kernel of its stream (launched with
+// the programmatic-serialization attribute) start before it finishes; that kernel waits for
+// the grids it depends on, and for their memory operations, at pdl_wait().  Without the
+// attribute both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Bulk prefetch of a global range into L2 (16-byte aligned address, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 // ----------------------------------------------------------------- small helpers
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -495,6 +495,7 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_swiglu_kernel(const T* __r
                                                                     int64_t pos) {
   constexpr int NW = DEC_THREADS / 32;
   __shared__ float part[NW][NB][RMAX][2];
+  pdl_launch_dependents();  // the apply may start prefetching its weights now
   if (H_buf != nullptr) {
     const int64_t per_row = d / 8;
     const int64_t nvec = (int64_t)Bc * mc * per_row;
@@ -583,14 +584,21 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_swiglu_kernel(const T* __r
 // O[b, t, e] = sum_n Z[b, t, n] * W[b, e, n] for the R <= RMAX rows t of each of the Bq
 // sequences: Z [Bq, R, f], W [Bq, d, f] (each sequence's current chunk weight), O [Bq, R, d].
 // A block takes NB rows e of one sequence at a time (d % NB == 0), split over its warps as in
-// decode_swiglu_kernel.
+// decode_swiglu_kernel.  Launched as a dependent of the SwiGLU rows, it first prefetches its
+// weight rows into L2 (when `prefetch`: the weights fit in L2 beside what the SwiGLU streams),
+// then waits for Z.
 template <typename T, int RMAX, int NB, int NBATCH>
 __global__ void __launch_bounds__(DEC_THREADS) decode_apply_kernel(const T* __restrict__ Z, const T* __restrict__ W,
-                                                                   T* __restrict__ O, int Bq, int R, int d, int f) {
+                                                                   T* __restrict__ O, int Bq, int R, int d, int f,
+                                                                   int prefetch) {
   constexpr int NW = DEC_THREADS / 32;
   __shared__ float part[NW][NB][RMAX];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t groups = (int64_t)Bq * d / NB;
+  if (prefetch && (int)threadIdx.x < NB)
+    for (int64_t q = blockIdx.x; q < groups; q += gridDim.x)
+      prefetch_l2_bulk(W + (q * NB + threadIdx.x) * f, (uint32_t)((int64_t)f * sizeof(T)));
+  pdl_wait();
   for (int64_t q = blockIdx.x; q < groups; q += gridDim.x) {
     const int64_t row0 = q * NB;  // rows row0 .. row0+NB-1 of the [Bq*d, f] weight stack
     const int64_t b = row0 / d;
