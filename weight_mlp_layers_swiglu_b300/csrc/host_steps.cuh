@@ -9,8 +9,10 @@ namespace {
 
 // ------------------------------------------------------------------ step launchers (no validation)
 
+// allow_pairs = false keeps the single-CTA tiles (bit-identical results); a few rows then take
+// d_ff/128 tiles in one wave over the SMs instead of two waves of pair tiles.
 ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const void* Wu, int64_t rows, int64_t d,
-                        int64_t f, ipttt_dtype dt, void* Z) {
+                        int64_t f, ipttt_dtype dt, void* Z, bool allow_pairs = true) {
   if (rows == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
     CUtensorMap ma, mb0, mb1, mo;
@@ -18,7 +20,7 @@ ipttt_status run_swiglu(ipttt_ctx* ctx, const void* H, const void* Wg, const voi
         !map_2d(ctx, &mb1, Wu, f, d, 64, 128) || !map_2d(ctx, &mo, Z, rows, f, 64, 32))
       return IPTTT_ERR_CUDA;
     gemm::Params p{};
-    const bool pairs = use_pairs(ctx);
+    const bool pairs = allow_pairs && use_pairs(ctx);
     p.m_tiles = ceil_div(rows, pairs ? gemm2::PAIR_M : gemm::BM);
     p.n_tiles = ceil_div(f, 128);
     p.k_blocks = ceil_div(d, gemm::BK);
@@ -450,7 +452,7 @@ ipttt_status run_decode_rows(ipttt_ctx* ctx, const void* H, const void* X0, cons
         return cuda_fail(ctx, e, "decode chunk buffers");
     }
     if ((s = ensure_attrs(ctx)) != IPTTT_OK) return s;
-    if ((s = run_swiglu(ctx, H, Wg, Wu, rows, d, f, IPTTT_BF16, Z)) != IPTTT_OK) return s;
+    if ((s = run_swiglu(ctx, H, Wg, Wu, rows, d, f, IPTTT_BF16, Z, rows > gemm::BM)) != IPTTT_OK) return s;
   }
   // the apply starts as a dependent launch: it prefetches W_cur into L2 while the SwiGLU rows
   // stream theirs (when W_cur takes at most half the L2), then waits for Z
