@@ -60,7 +60,7 @@ def _rank_main(rank, world, port, T_r, q):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world,T_r", [(2, 24), (3, 16), (3, 24)])
+@pytest.mark.parametrize("world,T_r", [(2, 24), (3, 16), (3, 24), (4, 16), (2, 40)])
 def test_gloo_ranks_equal_the_single_process_layer(world, T_r):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
