@@ -482,7 +482,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Z[r, n] = SiLU(H[r] . W_gate[n]) * (H[r] . W_up[n]) for the R <= RMAX rows of H [R, d].
 // A block takes NB columns n at a time; its 8 warps split each dot product over interleaved
 // 256-element slices of d (warp w: slices w, w+8, ...), with NB*NBATCH slices' weight loads in
-// flight per lane, and the warps' partial sums meet in shared memory in warp order.
+// flight per lane, and the warps' partial sums meet in shared memory in warp order.  The
+// block's weight rows are prefetched into L2 up front.
 // The first launch of a step may also copy the step's tokens into the chunk buffers:
 // H_buf[b, pos + t] = Hc[b, t] and X0_buf[b, pos + t] = X0c[b, t] for b < Bc, t < mc
 // ([Bc, mc, d] in, [Bc, C, d] buffers; H_buf NULL: no copy).
@@ -511,6 +512,14 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_swiglu_kernel(const T* __r
     }
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // every weight row this block will stream, queued at once as bulk L2 prefetches: the DRAM
+  // then works through one deep queue, whatever the loads in flight per lane
+  if ((int)threadIdx.x < 2 * NB)
+    for (int n0 = blockIdx.x * NB; n0 < f; n0 += gridDim.x * NB) {
+      const int c = threadIdx.x % NB;
+      if (n0 + c < f)
+        prefetch_l2_bulk(((int)threadIdx.x < NB ? Wg : Wu) + (int64_t)(n0 + c) * d, (uint32_t)((int64_t)d * sizeof(T)));
+    }
   for (int n0 = blockIdx.x * NB; n0 < f; n0 += gridDim.x * NB) {
     float ag[NB][RMAX], au[NB][RMAX];
 #pragma unroll
