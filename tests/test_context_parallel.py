@@ -98,3 +98,34 @@ def test_emulated_ranks_and_the_prefix():
     # the halo is the previous range's last k-1 rows
     X = torch.arange(2 * 5 * 3, dtype=torch.float64).reshape(2, 5, 3)
     assert torch.equal(cp.halo_rows(X, 3), X[:, 3:])
+
+
+def test_library_locals_keep_step_one_buffers_in_order():
+    """The library glue on a stand-in context: Step 3 takes the Z and V that Step 1 kept, range
+    by range in Step 1's order, and refuses a range whose length differs."""
+
+    class FakeCtx:
+        def __init__(self):
+            self.calls = []
+
+        def layer_totals(self, H_r, X0_r, W_gate, W_up, W_target, conv_w, halo, C, eta):
+            buf = torch.full((4,), float(len(self.calls)))
+            self.calls.append(("totals", H_r.shape[1]))
+            return torch.zeros(H_r.shape[0], 2, 3), buf
+
+        def layer_apply_saved(self, W_init, T, C, saved, dtype):
+            self.calls.append(("apply", T, float(saved[0])))
+            return torch.zeros(W_init.shape[0], T, 2, dtype=dtype), W_init
+
+    fake = FakeCtx()
+    lt, lr = cp.library_locals(fake, None, None, None, None, 8, 0.1)
+    H = [torch.zeros(2, n, 2) for n in (16, 8)]
+    for h in H:
+        lt(h, h, None)
+    W = torch.zeros(2, 2, 3)
+    lr(H[0], H[0], W, None)
+    lr(H[1], H[1], W, None)
+    assert fake.calls == [("totals", 16), ("totals", 8), ("apply", 16, 0.0), ("apply", 8, 1.0)]
+    lt(H[0], H[0], None)
+    with pytest.raises(ValueError):
+        lr(H[1], H[1], W, None)
