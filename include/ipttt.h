@@ -35,6 +35,8 @@
  *     context's limit makes the kernel record IPTTT_ERR_TIMEOUT and return; the code is
  *     reported by the next ipttt_sync().  No call throws or aborts the process.
  *   - Every failing call stores a message retrievable with ipttt_last_error().
+ *   - A context is used by one host thread at a time (calls on one context are not
+ *     synchronised with each other); separate contexts may be used from separate threads.
  */
 #ifndef IPTTT_H
 #define IPTTT_H
