@@ -36,7 +36,8 @@
  *     reported by the next ipttt_sync().  No call throws or aborts the process.
  *   - Every failing call stores a message retrievable with ipttt_last_error().
  *   - A context is used by one host thread at a time (calls on one context are not
- *     synchronised with each other); separate contexts may be used from separate threads.
+ *     synchronised with each other); separate contexts may be used from separate threads
+ *     (ipttt_target_noalloc, which takes no context, shares one scratch: see there).
  */
 #ifndef IPTTT_H
 #define IPTTT_H
