@@ -254,7 +254,8 @@ def run_ours(args, w):
     if world > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl", device_id=dev)
+        if not dist.is_initialized():  # a sweep runs several workloads in one process group
+            dist.init_process_group("nccl", device_id=dev)
     # this rank's batch: the workload's own batch, sequences offset by rank * B
     weights = {k: v.to(dev) for k, v in make_weights(w).items()}
     Hs, Xs = [], []
@@ -740,6 +741,16 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.tokens is not None:
         w = w.with_(name=f"{w.name}_T{args.tokens}", T=args.tokens)
+    try:
+        return dispatch(args, w)
+    finally:
+        import torch.distributed as dist
+
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+
+
+def dispatch(args, w) -> int:
     if args.impl == "reference":
         return run_reference(args, w)
     if args.cp:
