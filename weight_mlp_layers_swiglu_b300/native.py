@@ -569,7 +569,7 @@ class StreamingLayer:
       * tokens of a chunk that is not complete yet are applied at once with the weight at the
         chunk's start, and their inputs are buffered; when the chunk completes, its update is
         committed by running the resumable layer over the buffered chunk (the C-token buffer of
-        a decode loop).  Up to 8 such tokens per call go through ipttt_decode_step (the CUDA-core
+        a decode loop).  Up to 8 such tokens per call go through ipttt_decode_step (weight-streaming
         decode rows); more, or all of them with exact=True, through the SwiGLU step and the chunk
         apply, the tensor-core kernels of the chunked call.
     The state after every complete chunk equals that of one call over the whole sequence bit for
