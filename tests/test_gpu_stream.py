@@ -219,3 +219,29 @@ def test_state_weight_rounds_the_state(ctx):
     W32 = ctx.state_weight(W_state, torch.float32)
     assert ctx.sync() == 0
     assert torch.equal(W, W_state.to(torch.bfloat16)) and torch.equal(W32, W_state)
+
+
+def test_decode_step_edge_cases(ctx):
+    import weight_mlp_layers_swiglu_b300 as pkg
+
+    d, f = 64, 128
+    W = seeded((f, d), 0.1, torch.float32, 5, "cuda")
+    # no sequences: nothing to do
+    O, Z = ctx.decode_step(torch.empty((0, 1, d), device="cuda"), W, W, torch.empty((0, d, f), device="cuda"))
+    assert ctx.sync() == 0 and O.shape == (0, 1, d) and Z.shape == (0, 1, f)
+    # no tokens: unsupported (a step takes 1..8)
+    with pytest.raises(pkg.IptttError) as e:
+        ctx.decode_step(torch.empty((1, 0, d), device="cuda"), W, W, seeded((1, d, f), 0.1, torch.float32, 6, "cuda"))
+    assert e.value.status == 2
+    # fp32 with the chunk buffers: the stored rows are exact copies
+    H = seeded((3, 2, d), 1.0, torch.float32, 7, "cuda")
+    X0 = seeded((3, 2, d), 0.02, torch.float32, 8, "cuda")
+    Hb = torch.zeros((3, 5, d), device="cuda")
+    Xb = torch.zeros((3, 5, d), device="cuda")
+    Wc = seeded((3, d, f), f ** -0.5, torch.float32, 9, "cuda")
+    O, Z = ctx.decode_step(H, W, W, Wc, X0, Hb, Xb, pos=3)
+    assert ctx.sync() == 0, ctx.last_error()
+    assert torch.equal(Hb[:, 3:], H) and torch.equal(Xb[:, 3:], X0) and not Hb[:, :3].any() and not Xb[:, :3].any()
+    for b in range(3):
+        Z_ref = oracle.swiglu(H[b].cpu(), W.cpu(), W.cpu())
+        assert rel_err(O[b], oracle.chunk_apply(Z_ref, Wc[b].cpu()[None], 2)) <= TOL["f32"]
