@@ -108,7 +108,11 @@ ipttt_status ipttt_set_cta_pairs(ipttt_ctx* ctx, int enable);
 /* Ablation variant of the target (zhichai.net page §6, conv/proj ablation; its Theorem 1 uses
  * the next token's embedding as target): shift = 1 moves the conv window one token later, so
  * that the target of token t ends at X0[t+1] (the token after a call's last one reads as
- * zero, so split calls no longer match one call); shift = 0 (default) is the causal window.
+ * zero); shift = 0 (default) is the causal window.  A piece of a sequence would need the
+ * next piece's first X0 row for its last target, so with shift = 1 the entry points that
+ * run a sequence in pieces return UNSUPPORTED: ipttt_layer_forward_resume,
+ * ipttt_layer_totals, and ipttt_layer_forward_host when T spans more than one of its
+ * pieces.  ipttt_layer_forward, ipttt_target and the backward pass take it.
  * The other ablations need no switch: W_target = NULL is "w/o Proj" (identity projection;
  * the projection GEMM is skipped), k = 1 with conv_w = 1 is "w/o Conv". */
 ipttt_status ipttt_set_target_shift(ipttt_ctx* ctx, int shift);

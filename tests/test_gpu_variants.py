@@ -83,3 +83,48 @@ def test_target_step_without_projection(ctx):
     assert st == 0 and ctx.sync() == 0
     for b in range(2):
         assert rel_err(V[b], 0.5 * oracle.causal_conv(X0[b].cpu(), cw.cpu())) <= 1e-2
+
+
+def test_next_token_window_refused_by_piecewise_entry_points(ctx):
+    """The shifted window's last target of a piece reads the next piece's first X0 row, which a
+    piecewise call does not have: resumed calls, layer_totals and a host-buffer call that spans
+    several pieces refuse it (UNSUPPORTED) and launch nothing, while a host-buffer call of one
+    piece is one whole call and matches ipttt_layer_forward bit for bit."""
+    import weight_mlp_layers_swiglu_b300 as pkg
+
+    w, x = random_case(1, 512, 256, 512, 128, 4, 4.0 / 128, "bf16", 64)
+    xd = to_dev(x)
+    B, T, d, f, k = w.B, w.T, w.d, w.d_ff, w.k
+    W_state = xd["W_down0"].float()[None].repeat(B, 1, 1).contiguous()
+    ctx.set_target_shift(1)
+    try:
+        with pytest.raises(pkg.IptttError) as e:
+            ctx.layer_resume(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], W_state,
+                             None, w.C, w.eta)
+        assert e.value.status == 2  # IPTTT_ERR_UNSUPPORTED
+        with pytest.raises(pkg.IptttError) as e:
+            ctx.layer_totals(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], None, w.C,
+                             w.eta)
+        assert e.value.status == 2
+        # one piece: the whole call
+        O_pin = torch.empty((B, T, d), dtype=torch.bfloat16).pin_memory()
+        W_pin = torch.empty((B, d, f), dtype=torch.float32).pin_memory()
+        ctx.layer_forward_host(x["H"].pin_memory(), x["X0"].pin_memory(), xd["W_gate"], xd["W_up"], xd["W_down0"],
+                               xd["W_target"], xd["conv_w"], w.C, w.eta, O_pin, W_pin)
+        assert ctx.sync() == 0, ctx.last_error()
+        O, Wf = ctx.layer_forward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
+                                  xd["conv_w"], w.C, w.eta)
+        assert ctx.sync() == 0
+        assert torch.equal(O_pin, O.cpu()) and torch.equal(W_pin, Wf.cpu())
+        # several pieces: refused
+        wl, xl = random_case(1, 8192, 128, 256, 128, 4, 1.0 / 128, "bf16", 65)
+        xld = to_dev(xl)
+        Ol = torch.empty((1, 8192, 128), dtype=torch.bfloat16).pin_memory()
+        Wl = torch.empty((1, 128, 256), dtype=torch.float32).pin_memory()
+        with pytest.raises(pkg.IptttError) as e:
+            ctx.layer_forward_host(xl["H"].pin_memory(), xl["X0"].pin_memory(), xld["W_gate"], xld["W_up"],
+                                   xld["W_down0"], xld["W_target"], xld["conv_w"], wl.C, wl.eta, Ol, Wl)
+        assert e.value.status == 2
+    finally:
+        ctx.set_target_shift(0)
+    assert ctx.sync() == 0

@@ -36,8 +36,8 @@ def test_full_size_workload(ctx, name):
     ctx._ws = None
     torch.cuda.empty_cache()
     errs = layer_check(w, x, O, Wf)
-    out = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
-    if os.path.isdir(out):
+    out = os.environ.get("IPTTT_RESULTS_DIR")  # optional: a directory for the measured errors
+    if out and os.path.isdir(out):
         with open(os.path.join(out, f"parity_{name}.json"), "w") as f:
             json.dump({"workload": name, **errs}, f)
     print(name, errs)

@@ -400,6 +400,10 @@ ipttt_status ipttt_layer_totals(ipttt_ctx* ctx, const void* H, const void* X0, c
                                 int64_t d, int64_t d_ff, int64_t C, int k, float eta, ipttt_dtype dt, float* S,
                                 void* saved, size_t saved_bytes) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  if (ctx->target_shift != 0) {
+    set_err(ctx, "the shifted target window needs the next rank's first X0 row: not supported by layer_totals");
+    return IPTTT_ERR_UNSUPPORTED;
+  }
   const SavedLayout SL = saved_layout(B, T, d, d_ff, C, dt);
   ipttt_status s = check_shape(ctx, B, T, d, d_ff, C, k, dt);
   if (s != IPTTT_OK) return s;
@@ -514,6 +518,10 @@ ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const voi
                                         int64_t d_ff, int64_t C, int k, float eta, ipttt_dtype dt, void* O,
                                         float* W_state_out, void* X0_halo_out, void* ws, size_t ws_bytes) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  if (ctx->target_shift != 0) {
+    set_err(ctx, "the shifted target window needs the next call's first X0 row: not supported by resumed calls");
+    return IPTTT_ERR_UNSUPPORTED;
+  }
   // the shared-weight checks of the plain layer, with W_state standing in for W_down0
   ipttt_status s = validate_layer(ctx, H, X0, W_gate, W_up, W_state, W_target, conv_w, B, T, d, d_ff, C, k, eta, dt,
                                   O, W_state_out, ws, ws_bytes, false);
@@ -580,6 +588,11 @@ ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const 
   const size_t es = esize(dt);
   const HostLayout HL = host_layout(B, T, d, d_ff, C, k, dt);
   const int64_t P = HL.piece;
+  if (ctx->target_shift != 0 && T > P) {
+    set_err(ctx, "the shifted target window needs the next piece's first X0 row: T=%lld spans pieces of %lld tokens",
+            (long long)T, (long long)P);
+    return IPTTT_ERR_UNSUPPORTED;
+  }
   const size_t layer_ws = ws_layout(B, P, d, d_ff, C, dt).total;
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint8_t* Hd = base + HL.h;
@@ -872,6 +885,7 @@ struct NoAllocDevice {
   uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on that device
   EncodeTiledFn encode = nullptr;
   int sm_count = 0;
+  int pair_ctas = 0;  // CTAs of a CTA-pair grid on that device (0: the single-CTA kernels run)
 };
 
 NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
@@ -899,12 +913,16 @@ ipttt_status noalloc_device(int dev, NoAllocDevice* out) {
       cudaGetLastError();
       return IPTTT_ERR_CUDA;
     }
-    ipttt_ctx probe;  // holds nothing on the device; only used to set the kernel attributes
+    // holds nothing on the device: it sets the kernel attributes and sizes the CTA-pair grids
+    // (which need the SM count) exactly as ipttt_create's context does
+    ipttt_ctx probe;
     probe.device = dev;
+    probe.sm_count = sms;
     if (ensure_attrs(&probe) != IPTTT_OK) return IPTTT_ERR_CUDA;
     nd.scratch = static_cast<uint8_t*>(addr);
     nd.encode = reinterpret_cast<EncodeTiledFn>(fn);
     nd.sm_count = sms;
+    nd.pair_ctas = probe.pair_ctas;
     nd.ready = true;
   }
   *out = nd;
@@ -947,6 +965,7 @@ extern "C" ipttt_status ipttt_target_noalloc(const void* X0, const void* conv_w,
   c.sm_count = nd.sm_count;
   c.status = word;
   c.encode = nd.encode;
+  c.pair_ctas = nd.pair_ctas;
   c.attrs_set = true;
   void* Y = nd.scratch + kNoAllocStatusBytes;
   if ((s = run_conv(&c, X0, conv_w, B, T, d, k, dtype, Y)) != IPTTT_OK) return s;
