@@ -454,10 +454,10 @@ def run_cp(args, w):
     X0 = x["X0"][:, lo:hi].contiguous().to(dev)
     wd = {k: v.to(dev) for k, v in x.items() if k not in ("H", "X0")}
     ctx = pkg.Context(local)
-    lt, lr = cp.library_locals(ctx, wd["W_gate"], wd["W_up"], wd["W_target"], wd["conv_w"], w.C, w.eta)
+    lt, lr, ps = cp.library_locals(ctx, wd["W_gate"], wd["W_up"], wd["W_target"], wd["conv_w"], w.C, w.eta)
 
     def step():
-        return cp.cp_forward(H, X0, wd["W_down0"], w.k, lt, lr)
+        return cp.cp_forward(H, X0, wd["W_down0"], w.k, w.C, lt, lr, ps)
 
     for _ in range(args.warmup):
         step()
@@ -861,7 +861,7 @@ def main(argv=None):
                     help="override T (a shorter case of the same shapes, e.g. for profiler captures)")
     ap.add_argument("--cp", action="store_true",
                     help="context parallelism under torchrun: each rank holds a slice of every sequence "
-                         "(strong scaling; the exchange is one all_gather of the fp32 update totals)")
+                         "(strong scaling; the exchange is a rank-to-rank chain of the fp32 prefix states)")
     ap.add_argument("--sweep", choices=["chunk", "state"], default=None,
                     help="one line per chunk size C in {256, 512, 1024, 2048} (eta = 1/C) or per state size "
                          "d_ff in {0.5, 1, 4} x the workload's (the axes of the pages' ablations)")

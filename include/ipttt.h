@@ -185,8 +185,10 @@ ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const voi
  * continuing from X0_halo, the k-1 X0 rows before the range, NULL = zeros), Z and V go to
  * `saved` (the ipttt_saved_size() layout) and S[b] = eta * sum_i V_i^T Z_i [B, d, d_ff] fp32
  * is the range's update total, accumulated from zero with no per-chunk weight written.
- * Step 2 is the caller's exchange: the rank's starting state is W_down0 plus the totals of
- * the ranks before it.  Step 3, ipttt_layer_apply_saved: from that state W_init [B, d, d_ff]
+ * Step 2, ipttt_prefix_step: the rank's starting state is W_down0 plus the totals of the
+ * ranks before it, carried from rank to rank as a chain: rank 0's state is W_down0, and each
+ * rank adds its own total to the state it received and passes the sum on (the caller moves
+ * the buffers between ranks).  Step 3, ipttt_layer_apply_saved: from that state W_init [B, d, d_ff]
  * fp32 and the same `saved`, O [B, T, d] and the state after the range W_final [B, d, d_ff]
  * fp32 (W_final may be W_init itself); Z and V are not computed again.  Errors as the layer
  * calls. */
@@ -195,6 +197,21 @@ ipttt_status ipttt_layer_totals(ipttt_ctx* ctx, const void* H, const void* X0, c
                                 const void* X0_halo, int64_t B, int64_t T, int64_t d, int64_t d_ff,
                                 int64_t C, int k, float eta, ipttt_dtype dtype, float* S, void* saved,
                                 size_t saved_bytes);
+
+/* Step 2, one hop of the chain, on the elements [first, first + count) of the flattened
+ * [B, d, d_ff] fp32 state (so that a caller can pass the state on in pieces while later pieces
+ * are still arriving):
+ *   P_out[j] = base[j] + S[j],   base[j] = P_in[j], or W_down0[j mod (d * d_ff)] widened to
+ *                                fp32 when P_in is NULL (rank 0; the same W_down0 for every b)
+ *   P_in, S, P_out  [B, d, d_ff] fp32, device; S NULL = zeros (the state itself, e.g. rank 0's
+ *                   own starting state); P_out may be P_in or S itself (elementwise in place)
+ *   W_down0         [d, d_ff] dtype, device (read only when P_in is NULL)
+ * One fp32 addition per element, so every rank of a chain gets the sum of the totals before
+ * it in rank order whatever the pieces.  Errors: INVALID_ARG (NULL or misaligned pointers,
+ * a range outside the state, partial overlap), UNSUPPORTED (sizes as ipttt_layer_forward). */
+ipttt_status ipttt_prefix_step(ipttt_ctx* ctx, const float* P_in, const void* W_down0, const float* S,
+                               int64_t B, int64_t d, int64_t d_ff, ipttt_dtype dtype, int64_t first,
+                               int64_t count, float* P_out);
 
 ipttt_status ipttt_layer_apply_saved(ipttt_ctx* ctx, const float* W_init, int64_t B, int64_t T,
                                      int64_t d, int64_t d_ff, int64_t C, ipttt_dtype dtype, void* saved,

@@ -1,9 +1,9 @@
 """Context parallelism (the zhichai.net page's §3.2 three-step scheme) on CPU ranks.
 
 Each gloo rank holds a contiguous token range of every sequence and computes with the oracle;
-the exchange (one all_gather of the fp32 update totals, one of the k-1 halo rows) runs through
-weight_mlp_layers_swiglu_b300.context_parallel.  The concatenated outputs and the last rank's
-state must equal the oracle's single-process layer."""
+the exchange (the k-1 halo rows to the next rank, and Step 2 as a rank-to-rank chain of the
+prefix states, in pieces) runs through weight_mlp_layers_swiglu_b300.context_parallel.  The
+concatenated outputs and the last rank's state must equal the oracle's single-process layer."""
 import os
 import socket
 
@@ -35,6 +35,16 @@ def _oracle_locals(x, C, eta):
     return local_total, local_resume
 
 
+def _prefix_step(P_in, W_down0, S, P_out, first, count):
+    """Step 2's hop in float64 on CPU tensors (the test's stand-in for ipttt_prefix_step)."""
+    n = P_out.numel()
+    base = P_in.reshape(-1) if P_in is not None else W_down0.reshape(-1).to(P_out.dtype).repeat(n // W_down0.numel())
+    out = base[first:first + count].clone()
+    if S is not None:
+        out += S.reshape(-1)[first:first + count]
+    P_out.view(-1)[first:first + count] = out
+
+
 def _inputs():
     w, x = random_case(CASE["B"], CASE["T"], CASE["d"], CASE["f"], CASE["C"], CASE["k"], CASE["eta"], CASE["dtype"],
                        CASE["seed"])
@@ -47,31 +57,41 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _rank_main(rank, world, port, T_r, q):
+def _rank_main(rank, world, port, T_r, q, parts=8):
     import torch.distributed as dist
 
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     w, x = _inputs()
-    lo, hi = rank * T_r, min((rank + 1) * T_r, w.T)
+    lo, hi = min(rank * T_r, w.T), min((rank + 1) * T_r, w.T)
     lt, lr = _oracle_locals(x, w.C, w.eta)
-    O_r, W_r = cp.cp_forward(x["H"][:, lo:hi].contiguous(), x["X0"][:, lo:hi].contiguous(), x["W_down0"], w.k, lt, lr)
-    q.put((rank, O_r.numpy(), W_r.numpy()))
+    try:
+        O_r, W_r = cp.cp_forward(x["H"][:, lo:hi].contiguous(), x["X0"][:, lo:hi].contiguous(), x["W_down0"], w.k,
+                                 w.C, lt, lr, _prefix_step, parts=parts)
+        q.put((rank, O_r.numpy(), W_r.numpy()))
+    except ValueError as e:
+        q.put((rank, "ValueError", str(e)))
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world,T_r", [(2, 24), (3, 16), (3, 24), (4, 16), (2, 40)])
-def test_gloo_ranks_equal_the_single_process_layer(world, T_r):
+def _spawn(world, T_r, parts=8):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, world, port, T_r, q)) for r in range(world)]
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, T_r, q, parts)) for r in range(world)]
     for p in procs:
         p.start()
     got = sorted([q.get(timeout=180) for _ in procs], key=lambda t: t[0])
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
+    return got
+
+
+@pytest.mark.parametrize("world,T_r,parts", [(2, 24, 8), (3, 16, 8), (3, 24, 3), (4, 16, 8), (2, 40, 1),
+                                             (1, 48, 8)])
+def test_gloo_ranks_equal_the_single_process_layer(world, T_r, parts):
+    got = _spawn(world, T_r, parts)
     w, x = _inputs()
     O_ref, W_ref = oracle.layer_forward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"],
                                         x["conv_w"], w.C, w.eta)
@@ -82,22 +102,40 @@ def test_gloo_ranks_equal_the_single_process_layer(world, T_r):
     assert np.abs(got[last][2] - W_ref).max() / np.abs(W_ref).max() < 1e-12
 
 
-def test_emulated_ranks_and_the_prefix():
+def test_ranges_that_do_not_tile_whole_chunks_are_refused_on_every_rank():
+    """A non-final range that is not a multiple of C (here 20 tokens with C = 8), or an empty
+    range before a non-empty one, is refused by every rank alike before any data moves."""
+    for world, T_r in ((2, 20), (3, 4)):
+        got = _spawn(world, T_r)
+        assert all(g[1] == "ValueError" for g in got), got
+
+
+def test_range_checks():
+    cp.check_ranges([16, 16, 16], 8, 4)
+    cp.check_ranges([16, 5, 0, 0], 8, 4)  # the last non-empty range may be ragged; empty ones trail
+    for bad in ([12, 16], [16, 0, 8], [0, 8]):
+        with pytest.raises(ValueError):
+            cp.check_ranges(bad, 8, 4)
+    with pytest.raises(ValueError):  # shorter than the next rank's conv halo (k - 1 = 4 rows)
+        cp.check_ranges([2, 2], 2, 5)
+
+
+def test_emulated_ranks_and_the_chain():
     w, x = _inputs()
     lt, lr = _oracle_locals(x, w.C, w.eta)
-    O, W = cp.cp_forward_emulated(x["H"], x["X0"], x["W_down0"], w.k, 3, 16, lt, lr)
+    O, W = cp.cp_forward_emulated(x["H"], x["X0"], x["W_down0"], w.k, w.C, 3, 16, lt, lr, _prefix_step)
     O_ref, W_ref = oracle.layer_forward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"],
                                         x["conv_w"], w.C, w.eta)
     assert np.abs(O.numpy() - O_ref).max() / np.abs(O_ref).max() < 1e-12
     assert np.abs(W.numpy() - W_ref).max() / np.abs(W_ref).max() < 1e-12
-    # the prefix of rank r sums exactly the totals of ranks < r
-    totals = [torch.full((2, 3, 4), float(q + 1)) for q in range(4)]
-    W0 = torch.zeros(3, 4)
-    assert torch.equal(cp.exclusive_prefix(W0, totals, 0), torch.zeros(2, 3, 4))
-    assert torch.equal(cp.exclusive_prefix(W0, totals, 3), torch.full((2, 3, 4), 6.0))
     # the halo is the previous range's last k-1 rows
     X = torch.arange(2 * 5 * 3, dtype=torch.float64).reshape(2, 5, 3)
     assert torch.equal(cp.halo_rows(X, 3), X[:, 3:])
+    # the pieces tile the state, each a multiple of 4 elements but the last
+    for n in (1, 5, 64, 1001):
+        p = cp.pieces(n, 8)
+        assert p[0][0] == 0 and p[-1][1] == n and all(a[1] == b[0] for a, b in zip(p, p[1:]))
+        assert all((hi - lo) % 4 == 0 for lo, hi in p[:-1])
 
 
 def test_library_locals_keep_step_one_buffers_in_order():
@@ -118,7 +156,7 @@ def test_library_locals_keep_step_one_buffers_in_order():
             return torch.zeros(W_init.shape[0], T, 2, dtype=dtype), W_init
 
     fake = FakeCtx()
-    lt, lr = cp.library_locals(fake, None, None, None, None, 8, 0.1)
+    lt, lr, _ = cp.library_locals(fake, None, None, None, None, 8, 0.1)
     H = [torch.zeros(2, n, 2) for n in (16, 8)]
     for h in H:
         lt(h, h, None)

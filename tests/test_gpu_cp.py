@@ -1,8 +1,9 @@
 """Context parallelism on the GPU, ranks emulated one after another on one device (no kernel
-waits on another): the library computes each rank's total and its resumed range, the prefix
-and the halo are passed between them on the host side.  The result must meet the parity bar
-against the oracle, and stay close to one call of the layer (the per-rank totals sum the fp32
-state in a different order, so a few bf16 roundings may differ)."""
+waits on another): the library computes each rank's total, the chain of prefix states and
+each resumed range; the halo and the states are passed between them on the host side.  The
+result must meet the parity bar against the oracle, and stay close to one call of the layer
+(the per-rank totals sum the fp32 state in a different order, so a few bf16 roundings may
+differ)."""
 import pytest
 import torch
 
@@ -23,8 +24,8 @@ def test_emulated_ranks_match_one_call(dt, world, T_r):
     ctx = pkg.Context(0)
     O_ref, W_ref = ctx.layer_forward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
                                      xd["conv_w"], w.C, w.eta)
-    lt, lr = cp.library_locals(ctx, xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], w.C, w.eta)
-    O, W = cp.cp_forward_emulated(xd["H"], xd["X0"], xd["W_down0"], w.k, world, T_r, lt, lr)
+    lt, lr, ps = cp.library_locals(ctx, xd["W_gate"], xd["W_up"], xd["W_target"], xd["conv_w"], w.C, w.eta)
+    O, W = cp.cp_forward_emulated(xd["H"], xd["X0"], xd["W_down0"], w.k, w.C, world, T_r, lt, lr, ps)
     assert ctx.sync() == 0, ctx.last_error()
     ctx.close()
     from oracle import oracle
@@ -60,4 +61,36 @@ def test_totals_and_apply_saved_match_resume(dt, B, T, d, f, C, k):
     assert ctx.sync() == 0, ctx.last_error()
     assert torch.equal(S, S_ref)
     assert torch.equal(O, O_ref) and torch.equal(Wf, W_ref)
+    ctx.close()
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_prefix_step_is_one_fp32_addition_per_element(dt):
+    """ipttt_prefix_step: rank 0's state is W_down0 widened to fp32 and broadcast over the batch;
+    each later hop adds a total, elementwise and in place, over any range of the flattened
+    state: the same bits as torch's fp32 addition, also when applied in pieces of odd lengths
+    (the scalar path) and at offsets that are multiples of four (the vector path)."""
+    import weight_mlp_layers_swiglu_b300 as pkg
+    from tests.util import seeded
+
+    B, d, f = 3, 64, 136
+    ctx = pkg.Context(0)
+    W0 = seeded((d, f), f ** -0.5, dt, 1, "cuda")
+    S = seeded((B, d, f), 1e-2, torch.float32, 2, "cuda")
+    P0 = torch.full((B, d, f), float("nan"), device="cuda")
+    ctx.prefix_step(None, W0, None, P0)
+    P1 = torch.full_like(P0, float("nan"))
+    n = B * d * f
+    for lo, hi in [(0, 1000), (1000, 1003), (1003, 5001), (5001, n)]:
+        ctx.prefix_step(P0, W0, S, P1, lo, hi - lo)
+    S2 = S.clone()
+    ctx.prefix_step(P1, W0, S2, S2)  # in place into the total, as the chain forwards it
+    assert ctx.sync() == 0, ctx.last_error()
+    ref0 = W0.float()[None].expand(B, d, f)
+    assert torch.equal(P0, ref0)
+    assert torch.equal(P1, ref0 + S)
+    assert torch.equal(S2, (ref0 + S) + S)
+    # a range past the end launches nothing and reports INVALID_ARG
+    with pytest.raises(pkg.IptttError):
+        ctx.prefix_step(P0, W0, S, P1, n - 4, 8)
     ctx.close()

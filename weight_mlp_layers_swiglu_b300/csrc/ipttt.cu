@@ -512,6 +512,57 @@ ipttt_status ipttt_layer_apply_saved(ipttt_ctx* ctx, const float* W_init, int64_
                   &fuse);
 }
 
+ipttt_status ipttt_prefix_step(ipttt_ctx* ctx, const float* P_in, const void* W_down0, const float* S, int64_t B,
+                               int64_t d, int64_t d_ff, ipttt_dtype dt, int64_t first, int64_t count, float* P_out) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ipttt_status s = check_shape(ctx, B, 1, d, d_ff, 1, 1, dt, false);
+  if (s != IPTTT_OK) return s;
+  const int64_t n = B * d * d_ff;
+  if (first < 0 || count < 0 || first > n || count > n - first) {
+    set_err(ctx, "prefix_step: elements [%lld, %lld) outside the state of %lld", (long long)first,
+            (long long)(first + count), (long long)n);
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (count == 0) return IPTTT_OK;
+  if (!P_out || (!P_in && !W_down0)) {
+    set_err(ctx, "prefix_step: P_out and one of P_in / W_down0 are needed");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  auto al4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!al4(P_out) || (P_in && !al4(P_in)) || (S && !al4(S)) || (W_down0 && !al4(W_down0) && dt == IPTTT_F32) ||
+      (W_down0 && (reinterpret_cast<uintptr_t>(W_down0) & 1u))) {
+    set_err(ctx, "prefix_step: misaligned pointer");
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  // P_out may be P_in or S itself (element for element), but must not partly overlap them or W_down0
+  const size_t state = (size_t)n * 4;
+  std::vector<Region> all;
+  if (P_in && P_in != P_out) all.push_back({P_in, state, "P_in"});
+  if (S && S != P_out) all.push_back({S, state, "S"});
+  if (W_down0) all.push_back({W_down0, (size_t)d * d_ff * esize(dt), "W_down0"});
+  std::vector<Region> outs = {{P_out, state, "P_out"}};
+  std::string what;
+  if (find_overlap(outs, all, what)) {
+    set_err(ctx, "overlapping buffers: %s", what.c_str());
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  const int vec = (first % 4 == 0 && count % 4 == 0 && aligned16(P_out) && (!P_in || aligned16(P_in)) &&
+                   (!S || aligned16(S)))
+                      ? 1
+                      : 0;
+  const int64_t items = vec ? count / 4 : count;
+  const int64_t cap = (int64_t)ctx->sm_count * 8;
+  const int64_t blocks = ceil_div(items, 256) < cap ? ceil_div(items, 256) : cap;
+  if (dt == IPTTT_BF16)
+    simt::prefix_step_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, ctx->stream>>>(
+        P_in, static_cast<const __nv_bfloat16*>(W_down0), S, P_out, first, count, d * d_ff, vec);
+  else
+    simt::prefix_step_kernel<float><<<(unsigned)blocks, 256, 0, ctx->stream>>>(
+        P_in, static_cast<const float*>(W_down0), S, P_out, first, count, d * d_ff, vec);
+  return check_launch(ctx, "prefix step launch");
+}
+
 ipttt_status ipttt_layer_forward_resume(ipttt_ctx* ctx, const void* H, const void* X0, const void* W_gate,
                                         const void* W_up, const void* W_target, const void* conv_w,
                                         const float* W_state, const void* X0_halo, int64_t B, int64_t T, int64_t d,

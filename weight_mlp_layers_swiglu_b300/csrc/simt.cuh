@@ -422,6 +422,43 @@ __global__ void broadcast_state_kernel(const T* __restrict__ W0, float* __restri
   if (e < df) W_final[(int64_t)blockIdx.y * df + e] = static_cast<float>(W0[e]);
 }
 
+// One hop of the exclusive prefix over ranks (zhichai.net page, §3.2 Step 2), on elements
+// [first, first + count) of a flattened [B, d, d_ff] fp32 state:
+//   out[j] = base[j] + (S ? S[j] : 0),  base[j] = P_in ? P_in[j] : W0[j mod (d * d_ff)].
+// Vectors of four where the range allows (first and count multiples of 4, 16-byte aligned
+// pointers), single elements otherwise.  out may alias P_in or S element for element.
+template <typename T>
+__global__ void prefix_step_kernel(const float* P_in, const T* __restrict__ W0, const float* S, float* out,
+                                   int64_t first, int64_t count, int64_t df, int vec) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (vec) {
+    for (int64_t v = i0; v < count / 4; v += stride) {
+      const int64_t j = first + 4 * v;
+      float4 b;
+      if (P_in != nullptr) {
+        b = *reinterpret_cast<const float4*>(P_in + j);
+      } else {
+        const int64_t e = j % df;  // df % 4 == 0: the four elements stay in one row of W0
+        b = make_float4(static_cast<float>(W0[e]), static_cast<float>(W0[e + 1]), static_cast<float>(W0[e + 2]),
+                        static_cast<float>(W0[e + 3]));
+      }
+      if (S != nullptr) {
+        const float4 s = *reinterpret_cast<const float4*>(S + j);
+        b.x += s.x, b.y += s.y, b.z += s.z, b.w += s.w;
+      }
+      *reinterpret_cast<float4*>(out + j) = b;
+    }
+  } else {
+    for (int64_t v = i0; v < count; v += stride) {
+      const int64_t j = first + v;
+      float b = P_in != nullptr ? P_in[j] : static_cast<float>(W0[j % df]);
+      if (S != nullptr) b += S[j];
+      out[j] = b;
+    }
+  }
+}
+
 // The weight a chunk is applied with, from the running fp32 state: W[e] = T(state[e]) (bf16
 // round to nearest even, or an fp32 copy).
 template <typename T>

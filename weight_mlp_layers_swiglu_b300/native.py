@@ -66,6 +66,7 @@ _SIGNATURES = {
                                                                      c_vp, c_vp, ctypes.c_size_t]),
     "ipttt_layer_apply_saved": (ctypes.c_int, [c_vp, c_vp] + [c_i64] * 5 + [ctypes.c_int, c_vp, ctypes.c_size_t, c_vp,
                                                                              c_vp]),
+    "ipttt_prefix_step": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, c_i64, c_i64, c_vp]),
     "ipttt_swiglu": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, c_vp]),
     "ipttt_target": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 3 + [ctypes.c_int, ctypes.c_float, ctypes.c_int, c_vp, c_vp]),
     "ipttt_chunk_state": (ctypes.c_int, [c_vp] * 4 + [c_i64] * 5 + [ctypes.c_int, c_vp, c_vp]),
@@ -390,6 +391,25 @@ class Context:
                                               saved.numel() * saved.element_size(), _ptr(O), _ptr(W_final))
         self._check(st, "layer_apply_saved")
         return O, W_final
+
+    def prefix_step(self, P_in, W_down0, S, P_out, first: int = 0, count: int | None = None):
+        """Step 2, one hop: P_out = (P_in, or W_down0 broadcast when P_in is None) + S (None = 0) on
+        the flattened elements [first, first + count) of the [B, d, d_ff] fp32 state P_out."""
+        B, d, f = P_out.shape
+        dev = self.device
+        _need(P_out, "P_out", (B, d, f), torch.float32, dev)
+        if P_in is not None:
+            _need(P_in, "P_in", (B, d, f), torch.float32, dev)
+        if S is not None:
+            _need(S, "S", (B, d, f), torch.float32, dev)
+        if W_down0 is not None:
+            _need(W_down0, "W_down0", (d, f), W_down0.dtype, dev)
+        code = dtype_code(W_down0.dtype) if W_down0 is not None else F32
+        count = B * d * f - first if count is None else count
+        st = self.lib.ipttt_prefix_step(self.h, _ptr(P_in), _ptr(W_down0), _ptr(S), B, d, f, code, first, count,
+                                        _ptr(P_out))
+        self._check(st, "prefix_step")
+        return P_out
 
     def layer_resume(self, H, X0, W_gate, W_up, W_target, conv_w, W_state, X0_halo, C: int, eta: float,
                      O=None, W_state_out=None, X0_halo_out=None, workspace=None):
