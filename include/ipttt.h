@@ -62,12 +62,13 @@ typedef enum {
 
 typedef enum { IPTTT_F32 = 0, IPTTT_BF16 = 1 } ipttt_dtype;
 
-/* Kernel stages as reported by ipttt_timing_read().  The causal conv runs on an internal
- * side stream, forked from and joined back into the context's stream, and overlaps the
- * SwiGLU GEMM; its time is measured on that side stream. */
+/* Kernel stages as reported by ipttt_timing_read(), in the order a layer call runs them on
+ * the context's stream: the causal conv, the SwiGLU GEMM, the W_target projection, the
+ * chunk updates and the apply.  With step (2) as one kernel (ipttt_set_fused_target) the
+ * conv stage has zero length and the target stage holds both. */
 typedef enum {
   IPTTT_STAGE_SWIGLU = 0, /* step (1)                                     */
-  IPTTT_STAGE_CONV = 1,   /* causal conv of step (2), overlapping (1)     */
+  IPTTT_STAGE_CONV = 1,   /* causal conv of step (2), run before (1)       */
   IPTTT_STAGE_TARGET = 2, /* W_target projection of step (2), times eta   */
   IPTTT_STAGE_STATE = 3,  /* steps (3)+(4); with the fused kernel (3)-(5) */
   IPTTT_STAGE_APPLY = 4,  /* step (5); 0 with the fused kernel            */
@@ -81,10 +82,10 @@ const char* ipttt_version(void);
 const char* ipttt_status_string(ipttt_status s);
 
 /* Create a context on CUDA device `device`, bound to `cuda_stream` (a cudaStream_t; NULL =
- * the legacy default stream).  Allocates a 8-byte device status word, CUDA events and three
- * internal streams (the causal conv's side stream, and the upload and download streams of
- * ipttt_layer_forward_host), each ordered after and joined back into the context's stream by
- * events; this is the only call that allocates device memory.  *out receives the context.
+ * the legacy default stream).  Allocates a 8-byte device status word, CUDA events and two
+ * internal streams (the upload and download streams of ipttt_layer_forward_host), each
+ * ordered after and joined back into the context's stream by events; this is the only call
+ * that allocates device memory.  *out receives the context.
  * Errors: INVALID_ARG (out == NULL, bad device), CUDA. */
 ipttt_status ipttt_create(ipttt_ctx** out, int device, void* cuda_stream);
 
@@ -98,6 +99,17 @@ ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* cuda_stream);
  * cooperative launch, and calls whose cooperative grid no longer fits the SMs available to the
  * context, use two. */
 ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable);
+
+/* Choose how step (2) of a bf16 layer call runs: enable = 0 (default) as the conv kernel
+ * (memory bound, before step (1)) followed by the W_target GEMM; enable = 1 as one kernel on
+ * CTA pairs whose extra warps form each tile of the conv output Y = CausalConv1D(X0) in
+ * shared memory straight from X0 for the GEMM, so that Y is never stored.  Results are
+ * bit-identical: Y is the same fp32 fma chain rounded to bf16 either way.  The one-kernel form
+ * forms each Y tile once per 256-column block of V (d/256 times in all) on the CUDA cores, and
+ * at the 4B shape it is the slower of the two.  The training forward, calls without W_target
+ * and the single-CTA GEMMs always run the two kernels; ipttt_target always does (it returns
+ * Y). */
+ipttt_status ipttt_set_fused_target(ipttt_ctx* ctx, int enable);
 
 /* Choose how the bf16 GEMMs of steps (1), (2) and (5) run: enable = 1 (default) on CTA pairs
  * (clusters of two SMs issuing tcgen05.mma.cta_group::2 on 256-row tiles; the chunk apply
@@ -434,7 +446,8 @@ ipttt_status ipttt_timing_begin(ipttt_ctx* ctx);
 ipttt_status ipttt_timing_read(ipttt_ctx* ctx, double* ms, int64_t* calls, int64_t* launches);
 
 /* Number of kernels one ipttt_layer_forward call launches for this shape with the default
- * settings (host only): bf16 4 (fused steps 3-5), fp32 6; T = 0: 1; B = 0: 0. */
+ * settings (host only): bf16 3 (step (2) and steps (3)-(5) each one kernel), fp32 6; T = 0:
+ * 1; B = 0: 0. */
 int64_t ipttt_layer_launches(int64_t B, int64_t T, ipttt_dtype dtype);
 
 /* Launch one block that waits on a shared-memory barrier nothing ever signals, through

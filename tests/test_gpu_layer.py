@@ -165,13 +165,29 @@ def test_device_wait_limit_reports_timeout_and_context_survives(ctx):
 
 
 def test_timing_counts_launches(ctx):
+    import weight_mlp_layers_swiglu_b300 as pkg
+
     w, x = random_case(1, 512, 256, 512, 128, 4, 1.0 / 128, "bf16", 10)
     xd = to_dev(x)
-    ctx.timing_begin()
-    for _ in range(3):
-        ctx.layer_forward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
-                          xd["conv_w"], w.C, w.eta)
-    ms, calls, launches = ctx.timing_read()
+
+    def timed(fused_target):
+        ctx.set_fused_target(fused_target)
+        try:
+            ctx.timing_begin()
+            for _ in range(3):
+                ctx.layer_forward(xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"],
+                                  xd["conv_w"], w.C, w.eta)
+            return ctx.timing_read()
+        finally:
+            ctx.set_fused_target(False)
+
+    # the conv as a kernel of its own, then the target GEMM (the default)
+    ms, calls, launches = timed(False)
     assert calls == 3 and launches == 12  # SwiGLU, conv, target, fused state + apply
+    assert launches == 3 * pkg.layer_launches(w.B, w.T, pkg.BF16)
     assert ms["apply"] == 0.0
     assert all(ms[s] > 0 for s in ("swiglu", "conv", "target", "state"))
+    # step (2) as one kernel: the conv stage has zero length (event gaps only)
+    ms, calls, launches = timed(True)
+    assert calls == 3 and launches == 9
+    assert all(ms[s] > 0 for s in ("swiglu", "target", "state")) and ms["conv"] < 3 * 0.01

@@ -24,6 +24,7 @@
 #include "tc_gemm2.cuh"
 #include "tc_state.cuh"
 #include "tc_state2.cuh"
+#include "tc_target2.cuh"
 
 using namespace ipttt;
 
@@ -38,11 +39,11 @@ constexpr int kMaxPieces = 64;           // pieces of one host-buffer call
 constexpr int64_t kPieceTokens = 4096;   // target piece length (rounded up to a multiple of C)
 // Timing events recorded per timed layer call.
 enum : int {
-  kEvStart = 0,       // context stream, before the fork
-  kEvConvStart = 1,   // side stream
-  kEvConvEnd = 2,     // side stream
-  kEvSwigluEnd = 3,   // context stream
-  kEvJoined = 4,      // context stream, after waiting for the conv
+  kEvStart = 0,       // context stream, before the call's first kernel
+  kEvConvStart = 1,
+  kEvConvEnd = 2,     // the conv kernel (or nothing, when step (2) runs as one kernel)
+  kEvSwigluEnd = 3,
+  kEvJoined = 4,      // unused (kept for the event layout)
   kEvTargetEnd = 5,
   kEvStateEnd = 6,
   kEvApplyEnd = 7,
@@ -64,11 +65,8 @@ struct ipttt_ctx {
   bool cta_pairs = true;   // bf16 GEMMs on CTA pairs (cta_group::2) when the device allows
   int pair_ctas = 0;       // CTAs of the pair GEMM grid (2 x co-resident clusters; 0 = unavailable)
   bool fused_pairs = true; // the cooperative launch of the fused pair kernel has not been refused
+  bool fused_target = false;  // step (2) as one kernel (conv inside the target GEMM) when pairs run
   int target_shift = 0;    // 1: the conv window of the target ends at the next token
-  // The causal conv runs on an internal side stream, forked from and joined back into
-  // `stream` with these events, so that it overlaps the SwiGLU GEMM.
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
   // The host-buffer entry pipelines pieces of a call: uploads on copy_in and downloads on
   // copy_out overlap the compute on `stream` (per-piece events in piece_ev).
   cudaStream_t copy_in = nullptr, copy_out = nullptr;
@@ -208,7 +206,8 @@ ipttt_status check_launch(ipttt_ctx* ctx, const char* what) {
 
 bool encode_map(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                 const uint64_t* strides_bytes, const uint32_t* box,
-                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t gd[3], gs[2];
   cuuint32_t bx[3], es[3];
   for (int i = 0; i < rank; ++i) {
@@ -219,7 +218,7 @@ bool encode_map(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int rank, cons
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
   const CUresult r =
       ctx->encode(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_err(ctx, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -244,6 +243,16 @@ bool map_3d(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int
   const uint64_t strides[2] = {(uint64_t)inner * 2, (uint64_t)inner * mid * 2};
   const uint32_t box[3] = {64, box_mid, 1};
   return encode_map(ctx, m, base, 3, dims, strides, box);
+}
+
+// [outer, mid, inner] bf16 row-major, box = 64 inner x box_mid x 1, unswizzled (rows of 128
+// bytes one after another in shared memory, for CUDA-core readers).
+bool map_3d_plain(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int64_t mid, int64_t inner,
+                  uint32_t box_mid) {
+  const uint64_t dims[3] = {(uint64_t)inner, (uint64_t)mid, (uint64_t)outer};
+  const uint64_t strides[2] = {(uint64_t)inner * 2, (uint64_t)inner * mid * 2};
+  const uint32_t box[3] = {64, box_mid, 1};
+  return encode_map(ctx, m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // [outer, mid, inner] bf16 whose rows are row_stride elements apart (inner <= row_stride).
@@ -283,22 +292,36 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
                            gemm::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (two-segment)");
   {
-    const void* pk[7] = {(const void*)gemm2::tc_gemm2_kernel<gemm::kSwiglu>,
-                         (const void*)gemm2::tc_gemm2_kernel<gemm::kTarget>,
-                         (const void*)gemm2::tc_gemm2_kernel<gemm::kApply>,
-                         (const void*)gemm2::tc_gemm2_kernel<gemm::kSwigluSave>,
-                         (const void*)gemm2::tc_gemm2_kernel<gemm::kTwoSeg>, (const void*)state2::tc_state2_kernel,
-                         (const void*)fused2::tc_state_apply2_kernel};
-    const int pk_smem[7] = {gemm2::SMEM_BYTES, gemm2::SMEM_BYTES, gemm2::SMEM_BYTES, gemm2::SMEM_BYTES,
-                            gemm2::SMEM_BYTES, state2::SMEM_BYTES, fused2::SMEM_BYTES};
+    constexpr int NPK = 15;
+    const void* pk[NPK] = {(const void*)gemm2::tc_gemm2_kernel<gemm::kSwiglu>,
+                           (const void*)gemm2::tc_gemm2_kernel<gemm::kTarget>,
+                           (const void*)gemm2::tc_gemm2_kernel<gemm::kApply>,
+                           (const void*)gemm2::tc_gemm2_kernel<gemm::kSwigluSave>,
+                           (const void*)gemm2::tc_gemm2_kernel<gemm::kTwoSeg>,
+                           (const void*)state2::tc_state2_kernel,
+                           (const void*)fused2::tc_state_apply2_kernel,
+                           (const void*)tconv2::tc_target_conv2_kernel<1>,
+                           (const void*)tconv2::tc_target_conv2_kernel<2>,
+                           (const void*)tconv2::tc_target_conv2_kernel<3>,
+                           (const void*)tconv2::tc_target_conv2_kernel<4>,
+                           (const void*)tconv2::tc_target_conv2_kernel<5>,
+                           (const void*)tconv2::tc_target_conv2_kernel<6>,
+                           (const void*)tconv2::tc_target_conv2_kernel<7>,
+                           (const void*)tconv2::tc_target_conv2_kernel<8>};
+    int pk_smem[NPK], pk_threads[NPK];
+    for (int ki = 0; ki < NPK; ++ki) {
+      pk_smem[ki] = ki < 5 ? gemm2::SMEM_BYTES : ki == 5 ? state2::SMEM_BYTES : ki == 6 ? fused2::SMEM_BYTES
+                                                                                          : tconv2::SMEM_BYTES;
+      pk_threads[ki] = ki < 7 ? gemm2::NUM_THREADS : tconv2::NUM_THREADS;
+    }
     int clusters = 1 << 30;
-    for (int ki = 0; ki < 7; ++ki) {
+    for (int ki = 0; ki < NPK; ++ki) {
       const void* k = pk[ki];
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pk_smem[ki]);
       if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (pair kernels)");
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)(ctx->sm_count & ~1), 1, 1);
-      cfg.blockDim = dim3(gemm2::NUM_THREADS, 1, 1);
+      cfg.blockDim = dim3(pk_threads[ki], 1, 1);
       cfg.dynamicSmemBytes = pk_smem[ki];
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
@@ -322,6 +345,9 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
 DevStatus dev_status(ipttt_ctx* ctx) { return DevStatus{ctx->status, ctx->wait_limit_ns}; }
 
 bool use_pairs(const ipttt_ctx* ctx) { return ctx->cta_pairs && ctx->pair_ctas >= 2; }
+
+// Step (2) of a bf16 layer call runs as the one conv + projection kernel (tc_target2.cuh).
+bool use_fused_target(const ipttt_ctx* ctx) { return ctx->fused_target && use_pairs(ctx); }
 
 // Grid of a pair-GEMM launch: one CTA pair per tile, at most the co-resident pairs.
 int pair_grid(const ipttt_ctx* ctx, int64_t tiles) {

@@ -52,7 +52,9 @@ ipttt_status run_totals(ipttt_ctx* ctx, const void* H, const void* X0, const voi
   ipttt_status s = IPTTT_OK;
   if (dt == IPTTT_BF16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
   if ((s = run_swiglu(ctx, H, Wg, Wu, B * T, d, f, dt, sv.z)) != IPTTT_OK) return s;
-  if (Wt != nullptr) {
+  if (Wt != nullptr && dt == IPTTT_BF16 && use_fused_target(ctx)) {
+    if ((s = run_target_conv(ctx, X0, cw, Wt, B, T, d, k, eta, sv.v, halo_in)) != IPTTT_OK) return s;
+  } else if (Wt != nullptr) {
     if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, sv.y, halo_in)) != IPTTT_OK) return s;
     if ((s = run_target_gemm(ctx, sv.y, Wt, B * T, d, eta, dt, sv.v)) != IPTTT_OK) return s;
   } else if ((s = run_conv(ctx, X0, cw, B, T, d, k, dt, sv.v, halo_in, eta)) != IPTTT_OK) {
@@ -135,35 +137,33 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
     call = ctx->timed_calls++;
     ctx->timed_fused[call] = 0;
   }
-  cudaError_t e;
   mark(ctx, call, kEvStart, ctx->stream);
-  // fork: the causal conv (memory bound) overlaps the SwiGLU GEMM (tensor bound)
-  if ((e = cudaEventRecord(ctx->fork, ctx->stream)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(ctx->side, ctx->fork, 0)) != cudaSuccess)
-    return cuda_fail(ctx, e, "fork");
-  {
-    cudaStream_t main_stream = ctx->stream;
-    ctx->stream = ctx->side;
-    mark(ctx, call, kEvConvStart, ctx->side);
+  // Step (2) as one kernel (the conv inside the target GEMM, Y never stored) when selected,
+  // unless the training forward needs Y kept or the projection is left out; else the conv
+  // kernel first (memory bound, about 0.15 ms at the 4B shape and 32k tokens)
+  const bool fuse_target = Wt != nullptr && dt == IPTTT_BF16 && sv == nullptr && use_fused_target(ctx);
+  mark(ctx, call, kEvConvStart, ctx->stream);
+  if (!fuse_target) {
     // without W_target (the "w/o Proj" ablation) the conv writes V = eta * conv(X0) directly
     s = Wt != nullptr ? run_conv(ctx, X0, cw, B, T, d, k, dt, Y, halo_in)
                       : run_conv(ctx, X0, cw, B, T, d, k, dt, V, halo_in, eta);
-    mark(ctx, call, kEvConvEnd, ctx->side);
-    ctx->stream = main_stream;
     if (s != IPTTT_OK) return s;
   }
-  if ((e = cudaEventRecord(ctx->join, ctx->side)) != cudaSuccess) return cuda_fail(ctx, e, "join record");
+  mark(ctx, call, kEvConvEnd, ctx->stream);
   if ((s = sv ? run_swiglu_save(ctx, H, Wg, Wu, B * T, d, f, dt, Z, sv->au)
               : run_swiglu(ctx, H, Wg, Wu, B * T, d, f, dt, Z)) != IPTTT_OK)
     return s;
   mark(ctx, call, kEvSwigluEnd, ctx->stream);
-  if ((e = cudaStreamWaitEvent(ctx->stream, ctx->join, 0)) != cudaSuccess) return cuda_fail(ctx, e, "join");
   mark(ctx, call, kEvJoined, ctx->stream);
   const bool bf16 = dt == IPTTT_BF16;  // W_eff[b, 0] = W_down0: the apply reads W_down0 itself
   bool fuse = bf16 && ctx->fused_tail && ctx->coop;
   uint32_t* ctr = sv ? sv->ctr : reinterpret_cast<uint32_t*>(base + L.ctr);
   const int n_ctr = (int)(B * n_chunks_of(T, C) + 1);
-  if (Wt != nullptr) {
+  if (fuse_target) {
+    if ((s = run_target_conv(ctx, X0, cw, Wt, B, T, d, k, eta, V, halo_in, fuse ? ctr : nullptr, fuse ? n_ctr : 0)) !=
+        IPTTT_OK)
+      return s;
+  } else if (Wt != nullptr) {
     if ((s = run_target_gemm(ctx, Y, Wt, B * T, d, eta, dt, V, fuse ? ctr : nullptr, fuse ? n_ctr : 0)) != IPTTT_OK)
       return s;
   } else if (fuse) {
@@ -175,7 +175,8 @@ ipttt_status run_layer(ipttt_ctx* ctx, const void* H, const void* X0, const void
       IPTTT_OK)
     return s;
   if (call >= 0)
-    ctx->timed_launches += (bf16 ? (fuse ? 4 : 5) : 6) + ((halo_out != nullptr && k > 1) ? 1 : 0) - (Wt ? 0 : 1);
+    ctx->timed_launches += (bf16 ? (fuse ? 4 : 5) : 6) + ((halo_out != nullptr && k > 1) ? 1 : 0) - (Wt ? 0 : 1) -
+                           (fuse_target ? 1 : 0);
   return IPTTT_OK;
 }
 

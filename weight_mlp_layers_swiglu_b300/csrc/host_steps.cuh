@@ -78,8 +78,9 @@ void launch_conv(ipttt_ctx* ctx, dim3 grid, dim3 block, const void* X0, const vo
 ipttt_status run_conv(ipttt_ctx* ctx, const void* X0, const void* cw, int64_t B, int64_t T, int64_t d, int k,
                       ipttt_dtype dt, void* Y, const void* halo = nullptr, float scale = 1.f) {
   if (B == 0 || T == 0) return IPTTT_OK;
-  dim3 block(32, 4);
-  dim3 grid(ceil_div(d / 8, 32), ceil_div(T, (int64_t)simt::CONV_TS * 4), (unsigned)B);
+  const int rows = dt == IPTTT_BF16 ? simt::conv_rows<__nv_bfloat16>() : simt::conv_rows<float>();
+  dim3 block(32, simt::CONV_STRIPS);
+  dim3 grid(ceil_div(d / 8, 32), ceil_div(T, (int64_t)rows * simt::CONV_STRIPS), (unsigned)B);
   if (dt == IPTTT_BF16)
     launch_conv<__nv_bfloat16>(ctx, grid, block, X0, cw, Y, (int)T, (int)d, k, halo, ctx->target_shift, scale);
   else
@@ -132,6 +133,49 @@ ipttt_status run_target_gemm(ipttt_ctx* ctx, const void* Y, const void* Wt, int6
     p.scale = scale;
     dim3 grid(ceil_div(d, simt::SG_BN), ceil_div(rows, simt::SG_BM), 1);
     simt::sgemm_kernel<false><<<grid, 256, 0, ctx->stream>>>(p);
+  }
+  return check_launch(ctx, "target launch");
+}
+
+// Step (2) as one kernel on CTA pairs (tc_target2.cuh), bf16, W_target given:
+// V = scale * (CausalConv1D(X0) W_target), the conv window shifted by ctx->target_shift and
+// continuing from `halo` ([B, k-1, d], NULL = zeros); Y is never stored.  zero_ptr / zero_count:
+// words CTA 0 clears for the fused state + apply kernel that follows.
+ipttt_status run_target_conv(ipttt_ctx* ctx, const void* X0, const void* cw, const void* Wt, int64_t B, int64_t T,
+                             int64_t d, int k, float scale, void* V, const void* halo = nullptr,
+                             uint32_t* zero_ptr = nullptr, int zero_count = 0) {
+  if (B == 0 || T == 0) return IPTTT_OK;
+  CUtensorMap mx, mb, mo;
+  if (!map_3d_plain(ctx, &mx, X0, B, T, d, tconv2::XROWS) || !map_2d(ctx, &mb, Wt, d, d, 64, 64) ||
+      !map_3d(ctx, &mo, V, B, T, d, 32))
+    return IPTTT_ERR_CUDA;
+  tconv2::Params p{};
+  p.B = (int)B;
+  p.T = (int)T;
+  p.d = (int)d;
+  p.m_tiles = ceil_div(T, tconv2::PAIR_M);
+  p.n_tiles = ceil_div(d, tconv2::BN);
+  p.k_blocks = ceil_div(d, tconv2::BK);
+  p.group_m = 8;
+  p.shift = ctx->target_shift;
+  p.scale = scale;
+  p.conv_w = static_cast<const __nv_bfloat16*>(cw);
+  p.halo = k > 1 ? static_cast<const __nv_bfloat16*>(halo) : nullptr;
+  p.zero_ptr = zero_ptr;
+  p.zero_count = zero_count;
+  p.st = dev_status(ctx);
+  const int64_t tiles = (int64_t)p.B * p.m_tiles * p.n_tiles;
+  const dim3 grid((unsigned)pair_grid(ctx, tiles)), block(tconv2::NUM_THREADS);
+  const size_t sm = tconv2::SMEM_BYTES;
+  switch (k) {
+#define IPTTT_TCONV_CASE(KK) \
+  case KK: tconv2::tc_target_conv2_kernel<KK><<<grid, block, sm, ctx->stream>>>(mx, mb, mo, p); break;
+    IPTTT_TCONV_CASE(1) IPTTT_TCONV_CASE(2) IPTTT_TCONV_CASE(3) IPTTT_TCONV_CASE(4)
+    IPTTT_TCONV_CASE(5) IPTTT_TCONV_CASE(6) IPTTT_TCONV_CASE(7) IPTTT_TCONV_CASE(8)
+#undef IPTTT_TCONV_CASE
+    default:
+      set_err(ctx, "conv kernel size k=%d > %d", k, simt::CONV_MAXK);
+      return IPTTT_ERR_UNSUPPORTED;
   }
   return check_launch(ctx, "target launch");
 }

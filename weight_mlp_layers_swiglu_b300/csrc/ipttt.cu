@@ -62,10 +62,7 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
     delete ctx;
     return IPTTT_ERR_CUDA;
   }
-  if (cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ctx->fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ctx->join, cudaEventDisableTiming) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&ctx->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+  if (cudaStreamCreateWithFlags(&ctx->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&ctx->copy_out, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&ctx->h_fork, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&ctx->h_join, cudaEventDisableTiming) != cudaSuccess) {
@@ -114,6 +111,12 @@ ipttt_status ipttt_set_target_shift(ipttt_ctx* ctx, int shift) {
   return IPTTT_OK;
 }
 
+ipttt_status ipttt_set_fused_target(ipttt_ctx* ctx, int enable) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  ctx->fused_target = enable != 0;
+  return IPTTT_OK;
+}
+
 ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
   ctx->fused_tail = enable != 0;
@@ -157,9 +160,6 @@ void ipttt_destroy(ipttt_ctx* ctx) {
   DeviceGuard g(ctx->device);
   for (auto& e : ctx->events)
     if (e) cudaEventDestroy(e);
-  if (ctx->fork) cudaEventDestroy(ctx->fork);
-  if (ctx->join) cudaEventDestroy(ctx->join);
-  if (ctx->side) cudaStreamDestroy(ctx->side);
   for (auto& e : ctx->piece_ev)
     if (e) cudaEventDestroy(e);
   if (ctx->h_fork) cudaEventDestroy(ctx->h_fork);
@@ -880,11 +880,11 @@ ipttt_status ipttt_timing_read(ipttt_ctx* ctx, double* ms, int64_t* calls, int64
   DeviceGuard g(ctx->device);
   ctx->timing = false;
   for (int s = 0; s < IPTTT_NUM_STAGES; ++s) ms[s] = 0.0;
-  // stage intervals: swiglu [start, swiglu end], conv [conv start, conv end] on the side stream
-  // (overlapping the SwiGLU GEMM), target [joined, target end], state, apply
-  const int iv[IPTTT_NUM_STAGES][2] = {{kEvStart, kEvSwigluEnd},
+  // stage intervals, in stream order: conv [conv start, conv end], swiglu [conv end, swiglu
+  // end], target [swiglu end, target end], state, apply
+  const int iv[IPTTT_NUM_STAGES][2] = {{kEvConvEnd, kEvSwigluEnd},
                                        {kEvConvStart, kEvConvEnd},
-                                       {kEvJoined, kEvTargetEnd},
+                                       {kEvSwigluEnd, kEvTargetEnd},
                                        {kEvTargetEnd, kEvStateEnd},
                                        {kEvStateEnd, kEvApplyEnd}};
   for (int c = 0; c < ctx->timed_calls; ++c) {

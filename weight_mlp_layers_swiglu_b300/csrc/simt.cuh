@@ -15,25 +15,51 @@ namespace simt {
 
 // --------------------------------------------------------------------------- causal conv
 // Y[b, t, c] = sum_{s<k} conv_w[c, s] * X0[b, t-(k-1)+s, c], zero for t-(k-1)+s < 0
-// (zhichai.net page, §3.3: Conv1D with causal padding).  Each thread owns 8 channels and a
-// strip of CONV_TS tokens, keeping the last k-1 input rows in registers.
+// (zhichai.net page, §3.3: Conv1D with causal padding).  The conv reads and writes each
+// element once, so it is bound by memory bandwidth: each thread owns 8 channels (one 16- or
+// 32-byte vector) of a strip of conv_rows<T>() tokens and issues the loads of all its input
+// rows (the strip and the k-1 rows before it) before any arithmetic, so that every thread
+// keeps that many vector loads in flight.  The sum for one output is an fp32 fma chain over
+// the taps from zero, s = 0 .. k-1.
 constexpr int CONV_MAXK = 8;
-constexpr int CONV_TS = 32;
+constexpr int CONV_STRIPS = 4;  // token strips per block (blockDim.y); blockDim.x = 32 channel groups
 
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&v)[8]);
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+__host__ __device__ constexpr int conv_rows() {
+  return sizeof(T) == 2 ? 8 : 4;
 }
+
+// One row's 8 channels as loaded: a 16-byte vector (bf16) or two (fp32), widened when used.
+template <typename T>
+struct Row8;
 template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
-  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+struct Row8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void zero() { v = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ void widen(float (&f)[8]) const {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+  }
+};
+template <>
+struct Row8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void widen(float (&f)[8]) const {
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
+  Row8<T> r;
+  r.load(p);
+  r.widen(v);
 }
 template <typename T>
 __device__ __forceinline__ void store8(T* p, const float (&v)[8]);
@@ -57,51 +83,50 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const fl
 // token later (it ends at t+1; the token after the last one reads as zero).  The output is
 // multiplied by `scale`.
 template <typename T, int K>
-__global__ void causal_conv_kernel(const T* __restrict__ X0, const T* __restrict__ conv_w, T* __restrict__ Y,
-                                   int T_len, int d, const T* __restrict__ halo, int shift, float scale) {
-  const int cg = blockIdx.x * blockDim.x + threadIdx.x;  // channel group of 8
-  const int c0 = cg * 8;
-  const int t0 = (blockIdx.y * blockDim.y + threadIdx.y) * CONV_TS;
+__global__ void __launch_bounds__(32 * CONV_STRIPS, 4)
+    causal_conv_kernel(const T* __restrict__ X0, const T* __restrict__ conv_w, T* __restrict__ Y, int T_len, int d,
+                       const T* __restrict__ halo, int shift, float scale) {
+  constexpr int R = conv_rows<T>();
+  const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  const int t0 = (blockIdx.y * blockDim.y + threadIdx.y) * R;
   const int b = blockIdx.z;
   if (c0 >= d || t0 >= T_len) return;
+  const T* xb = X0 + (int64_t)b * T_len * d + c0;
+  T* yb = Y + (int64_t)b * T_len * d + c0;
+  // input row j is X0[t0 + shift - (K-1) + j]: issue every load first
+  Row8<T> raw[R + K - 1];
+#pragma unroll
+  for (int j = 0; j < R + K - 1; ++j) {
+    const int src = t0 + shift - (K - 1) + j;
+    if (src >= 0 && src < T_len)
+      raw[j].load(xb + (int64_t)src * d);
+    else if (src < 0 && halo != nullptr)
+      raw[j].load(halo + ((int64_t)b * (K - 1) + (K - 1) + src) * d + c0);
+    else
+      raw[j].zero();
+  }
   float w[8][K];
 #pragma unroll
   for (int e = 0; e < 8; ++e)
 #pragma unroll
     for (int s = 0; s < K; ++s) w[e][s] = static_cast<float>(conv_w[(int64_t)(c0 + e) * K + s]);
-  const T* xb = X0 + (int64_t)b * T_len * d + c0;
-  T* yb = Y + (int64_t)b * T_len * d + c0;
-  // win[s] holds X0[t+shift-(K-1)+s], s < K-1, while output t is formed; win[K-1] is X0[t+shift]
-  float win[K][8];
+  float win[K][8];  // the last K input rows, widened
 #pragma unroll
-  for (int s = 0; s < K - 1; ++s) {
-    const int src = t0 + shift - (K - 1) + s;
-    if (src >= 0 && src < T_len) {
-      load8<T>(xb + (int64_t)src * d, win[s]);
-    } else if (src < 0 && halo != nullptr) {
-      load8<T>(halo + ((int64_t)b * (K - 1) + (K - 1) + src) * d + c0, win[s]);
-    } else {
+  for (int j = 0; j < K - 1; ++j) raw[j].widen(win[j]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) win[s][e] = 0.f;
+  for (int r = 0; r < R; ++r) {
+    raw[r + K - 1].widen(win[K - 1]);
+    if (t0 + r < T_len) {
+      float out[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < K; ++s) acc = fmaf(w[e][s], win[s][e], acc);
+        out[e] = acc * scale;
+      }
+      store8<T>(yb + (int64_t)(t0 + r) * d, out);
     }
-  }
-  const int t_end = min(t0 + CONV_TS, T_len);
-  for (int t = t0; t < t_end; ++t) {
-    if (t + shift < T_len) {
-      load8<T>(xb + (int64_t)(t + shift) * d, win[K - 1]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) win[K - 1][e] = 0.f;
-    }
-    float out[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float acc = 0.f;
-#pragma unroll
-      for (int s = 0; s < K; ++s) acc = fmaf(w[e][s], win[s][e], acc);
-      out[e] = acc * scale;
-    }
-    store8<T>(yb + (int64_t)t * d, out);
 #pragma unroll
     for (int s = 0; s < K - 1; ++s)
 #pragma unroll

@@ -32,6 +32,7 @@ _SIGNATURES = {
     "ipttt_set_stream": (ctypes.c_int, [c_vp, c_vp]),
     "ipttt_set_wait_limit_ns": (ctypes.c_int, [c_vp, ctypes.c_uint64]),
     "ipttt_set_fused_tail": (ctypes.c_int, [c_vp, ctypes.c_int]),
+    "ipttt_set_fused_target": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_set_cta_pairs": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_set_target_shift": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_sync": (ctypes.c_int, [c_vp]),
@@ -205,6 +206,9 @@ class Context:
 
     def set_target_shift(self, shift: int):
         self._check(self.lib.ipttt_set_target_shift(self.h, int(shift)), "set_target_shift")
+
+    def set_fused_target(self, enable: bool):
+        self._check(self.lib.ipttt_set_fused_target(self.h, 1 if enable else 0), "set_fused_target")
 
     def set_fused_tail(self, enable: bool):
         self._check(self.lib.ipttt_set_fused_tail(self.h, 1 if enable else 0), "set_fused_tail")
