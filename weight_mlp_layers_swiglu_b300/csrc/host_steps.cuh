@@ -343,8 +343,12 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
   p.s.skip_first = (W_init == nullptr && !write_first) ? 1 : 0;
   p.s.W_init = W_init;
   p.s.st = dev_status(ctx);
+  // 256 x 512 apply tiles when they still make two waves over the co-resident pairs, else
+  // 256 x 256 tiles (twice as many) so that a short call keeps more pairs busy
+  const int64_t wide_tiles = B * n * (C / gemm2::PAIR_M) * ceil_div(d, 2 * gemm2::BN);
+  p.a_halves = wide_tiles >= (int64_t)ctx->pair_ctas ? 2 : 1;
   p.a.m_tiles = (int)(C / gemm2::PAIR_M);
-  p.a.n_tiles = ceil_div(d, gemm2::BN);
+  p.a.n_tiles = ceil_div(d, p.a_halves * gemm2::BN);
   p.a.k_blocks = ceil_div(f, gemm2::BK);
   p.a.problems = (int)(B * n);
   p.a.group_m = 8;
