@@ -836,9 +836,9 @@ def dominant_traffic(kernel: str, w):
 
 
 # The sources a tensor-core kernel's DRAM traffic depends on: the kernels themselves and the
-# launch configurations (tiles, rasterisation, grids) in the step launchers.
+# launch configurations (tiles, rasterisation, grids) in the step launchers, and the tensor maps.
 TRAFFIC_SOURCES = ("ptx.cuh", "tc_gemm.cuh", "tc_gemm2.cuh", "tc_state.cuh", "tc_state2.cuh", "tc_fused.cuh",
-                   "tc_fused2.cuh", "host_steps.cuh")
+                   "tc_fused2.cuh", "host_steps.cuh", "host_context.cuh")
 
 
 def source_digest(src_dir: str) -> str:

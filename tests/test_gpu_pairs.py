@@ -94,7 +94,10 @@ def test_layer_pairs_match_single(ctx, fused, B, T, d, f, C, k):
                                        (1, 5, 64, 64, 128), (3, 600, 1024, 4096, 256)])
 def test_chunk_state_pairs_match_single(ctx, reverse_case, B, T, d, f, C):
     """The state kernel on pairs (256-row units) and on single CTAs (128-row units); the reverse
-    scan is exercised through the backward pass."""
+    scan is exercised through the backward pass.  Widths that are multiples of 64 (192 x 384,
+    512 x 1024, 64 x 64, 1024 x 4096) give the pairs V and Z as blocks of 64 columns (one 4-D TMA
+    request per operand and k-block, d = 192 and d = 64 with the second block of a CTA past the
+    edge); 136 x 264 keeps the 3-D maps; the single CTAs always load 3-D maps."""
     if not reverse_case:
         V = seeded((B, T, d), 1.0, torch.bfloat16, 7, "cuda")
         Z = seeded((B, T, f), C ** -0.5, torch.bfloat16, 8, "cuda")

@@ -18,7 +18,8 @@ ipttt_status launch_state_general(ipttt_ctx* ctx, const void* V, int64_t v_strid
                                   const float* W_init, bool skip_first, bool reverse, void* W_eff, float* W_final) {
   const int64_t n = n_chunks_of(T, C);
   CUtensorMap mv, mz, mw, mf;
-  if (!map_3d_strided(ctx, &mv, V, B, T, M, v_stride, 64) || !map_3d_strided(ctx, &mz, Z, B, T, N, z_stride, 64) ||
+  int blocked = 0;
+  if (!map_state_operands(ctx, &mv, &mz, V, v_stride, Z, z_stride, B, T, M, N, use_pairs(ctx), &blocked) ||
       !map_3d_f32(ctx, &mf, W_final, B, M, N, 32))
     return IPTTT_ERR_CUDA;
   if (W_eff != nullptr) {
@@ -40,6 +41,7 @@ ipttt_status launch_state_general(ipttt_ctx* ctx, const void* V, int64_t v_strid
   p.skip_first = skip_first ? 1 : 0;
   p.W_init = W_init;
   p.reverse = reverse ? 1 : 0;
+  p.blocked = blocked;
   p.st = dev_status(ctx);
   return launch_state_kernel(ctx, mv, mz, mw, mf, p);
 }

@@ -208,8 +208,8 @@ bool encode_map(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int rank, cons
                 const uint64_t* strides_bytes, const uint32_t* box,
                 CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-  cuuint64_t gd[3], gs[2];
-  cuuint32_t bx[3], es[3];
+  cuuint64_t gd[4], gs[3];
+  cuuint32_t bx[4], es[4];
   for (int i = 0; i < rank; ++i) {
     gd[i] = dims[i];
     bx[i] = box[i];
@@ -253,6 +253,18 @@ bool map_3d_plain(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t oute
   const uint64_t strides[2] = {(uint64_t)inner * 2, (uint64_t)inner * mid * 2};
   const uint32_t box[3] = {64, box_mid, 1};
   return encode_map(ctx, m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// [outer, mid, inner] bf16 (rows row_stride elements apart, inner a multiple of 64) seen as
+// [outer][inner / 64][mid][64]: blocks of 64 columns.  The box is two blocks of 64 columns x
+// 64 rows, so one request brings what two requests of the 3-D map with box_mid = 64 bring, in
+// the same shared-memory layout (block 0's 64 rows of 128 bytes, then block 1's).
+bool map_blocks(ipttt_ctx* ctx, CUtensorMap* m, const void* base, int64_t outer, int64_t mid, int64_t inner,
+                int64_t row_stride) {
+  const uint64_t dims[4] = {64, (uint64_t)mid, (uint64_t)(inner / 64), (uint64_t)outer};
+  const uint64_t strides[3] = {(uint64_t)row_stride * 2, 128, (uint64_t)row_stride * mid * 2};
+  const uint32_t box[4] = {64, 64, 2, 1};
+  return encode_map(ctx, m, base, 4, dims, strides, box);
 }
 
 // [outer, mid, inner] bf16 whose rows are row_stride elements apart (inner <= row_stride).
@@ -345,6 +357,19 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
 DevStatus dev_status(ipttt_ctx* ctx) { return DevStatus{ctx->status, ctx->wait_limit_ns}; }
 
 bool use_pairs(const ipttt_ctx* ctx) { return ctx->cta_pairs && ctx->pair_ctas >= 2; }
+
+// The token-major operands of a state kernel (V: [B, T, M], Z: [B, T, N], rows v_stride and
+// z_stride elements apart) as the kernel loads them: for the CTA-pair kernels, with M and N
+// multiples of 64, as blocks of 64 columns (map_blocks, one request per operand and k-block;
+// p.blocked = 1), else as 3-D maps with 64-token boxes (two requests each).
+bool map_state_operands(ipttt_ctx* ctx, CUtensorMap* mv, CUtensorMap* mz, const void* V, int64_t v_stride,
+                        const void* Z, int64_t z_stride, int64_t B, int64_t T, int64_t M, int64_t N, bool pairs,
+                        int* blocked) {
+  *blocked = (pairs && M % 64 == 0 && N % 64 == 0) ? 1 : 0;
+  if (*blocked)
+    return map_blocks(ctx, mv, V, B, T, M, v_stride) && map_blocks(ctx, mz, Z, B, T, N, z_stride);
+  return map_3d_strided(ctx, mv, V, B, T, M, v_stride, 64) && map_3d_strided(ctx, mz, Z, B, T, N, z_stride, 64);
+}
 
 // Step (2) of a bf16 layer call runs as the one conv + projection kernel (tc_target2.cuh).
 bool use_fused_target(const ipttt_ctx* ctx) { return ctx->fused_target && use_pairs(ctx); }

@@ -64,7 +64,8 @@ ipttt_status run_totals(ipttt_ctx* ctx, const void* H, const void* X0, const voi
     return run_state(ctx, sv.v, sv.z, nullptr, B, T, d, f, C, dt, sv.wst, S, false, nullptr);
   const int64_t n = n_chunks_of(T, C);
   CUtensorMap mv, mz, mf;
-  if (!map_3d(ctx, &mv, sv.v, B, T, d, 64) || !map_3d(ctx, &mz, sv.z, B, T, f, 64) ||
+  int blocked = 0;
+  if (!map_state_operands(ctx, &mv, &mz, sv.v, d, sv.z, f, B, T, d, f, use_pairs(ctx), &blocked) ||
       !map_3d_f32(ctx, &mf, S, B, d, f, 32))
     return IPTTT_ERR_CUDA;
   state::Params p{};
@@ -79,6 +80,7 @@ ipttt_status run_totals(ipttt_ctx* ctx, const void* H, const void* X0, const voi
   p.units = (int)(B * p.m_units * p.n_units);
   p.skip_first = 1;
   p.no_snap = 1;  // zero start (W0 and W_init NULL), only the final state is stored
+  p.blocked = blocked;
   p.st = dev_status(ctx);
   return launch_state_kernel(ctx, mv, mz, mv, mf, p);
 }

@@ -190,6 +190,10 @@ ipttt_status launch_state_kernel(ipttt_ctx* ctx, const CUtensorMap& mv, const CU
     state2::tc_state2_kernel<<<pair_grid(ctx, (p.units + 1) / 2), state2::NUM_THREADS, state2::SMEM_BYTES,
                                ctx->stream>>>(mv, mz, mw, mf, p);
   } else {
+    if (p.blocked) {  // the single-CTA kernel loads 3-D maps only
+      set_err(ctx, "state kernel: blocked operand maps without CTA pairs");
+      return IPTTT_ERR_UNSUPPORTED;
+    }
     const int pairs = (p.units + 1) / 2;
     const int grid = pairs < ctx->sm_count ? pairs : ctx->sm_count;
     state::tc_state_kernel<<<grid, state::NUM_THREADS, state::SMEM_BYTES, ctx->stream>>>(mv, mz, mw, mf, p);
@@ -208,10 +212,12 @@ ipttt_status run_state(ipttt_ctx* ctx, const void* V, const void* Z, const void*
   if (B == 0 || n == 0) return IPTTT_OK;
   if (dt == IPTTT_BF16) {
     CUtensorMap mv, mz, mw, mf;
-    if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64) ||
+    int blocked = 0;
+    if (!map_state_operands(ctx, &mv, &mz, V, d, Z, f, B, T, d, f, use_pairs(ctx), &blocked) ||
         !map_3d(ctx, &mw, W_eff, B * n, d, f, 32) || !map_3d_f32(ctx, &mf, W_final, B, d, f, 32))
       return IPTTT_ERR_CUDA;
     state::Params p{};
+    p.blocked = blocked;
     p.B = (int)B;
     p.T = (int)T;
     p.d = (int)d;
@@ -318,8 +324,9 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
                               const float* W_init, bool write_first, ipttt_status* st) {
   const int64_t n = n_chunks_of(T, C);
   CUtensorMap mv, mz, mw_st, mf, mza, mw_ld, mw0, mo;
+  int blocked = 0;
   *st = IPTTT_ERR_CUDA;
-  if (!map_3d(ctx, &mv, V, B, T, d, 64) || !map_3d(ctx, &mz, Z, B, T, f, 64) ||
+  if (!map_state_operands(ctx, &mv, &mz, V, d, Z, f, B, T, d, f, true, &blocked) ||
       !map_3d(ctx, &mw_st, W_eff, B * n, d, f, 32) || !map_3d_f32(ctx, &mf, W_final, B, d, f, 32) ||
       !map_3d(ctx, &mza, Z, B, T, f, 128) || !map_3d(ctx, &mw_ld, W_eff, B * n, d, f, 128) ||
       !map_3d(ctx, &mo, O, B, T, d, 32))
@@ -342,6 +349,7 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
   p.s.W0 = static_cast<const __nv_bfloat16*>(W0);
   p.s.skip_first = (W_init == nullptr && !write_first) ? 1 : 0;
   p.s.W_init = W_init;
+  p.s.blocked = blocked;
   p.s.st = dev_status(ctx);
   // 256 x 512 apply tiles when they still make two waves over the co-resident pairs, else
   // 256 x 256 tiles (twice as many) so that a short call keeps more pairs busy

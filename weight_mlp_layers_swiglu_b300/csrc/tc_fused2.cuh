@@ -165,10 +165,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const uint32_t bar = cluster_addr(smem_u32(&full[p_stage]), 0);
             if (rank == 0) mbar_arrive_expect_tx(&full[p_stage], 2 * STAGE_BYTES);
             const int tok = i * S.C + kb * state2::BKT;
-            tma_load_3d_pair(sa, &map_v, bar, d0, tok, b);
-            tma_load_3d_pair(sa + state2::BKT * 128, &map_v, bar, d0 + 64, tok, b);
-            tma_load_3d_pair(sb, &map_z, bar, f0, tok, b);
-            tma_load_3d_pair(sb + state2::BKT * 128, &map_z, bar, f0 + 64, tok, b);
+            if (S.blocked) {  // the CTA's two 64-column blocks of V, then of Z, one request each
+              tma_load_4d_pair(sa, &map_v, bar, 0, tok, d0 >> 6, b);
+              tma_load_4d_pair(sb, &map_z, bar, 0, tok, f0 >> 6, b);
+            } else {
+              tma_load_3d_pair(sa, &map_v, bar, d0, tok, b);
+              tma_load_3d_pair(sa + state2::BKT * 128, &map_v, bar, d0 + 64, tok, b);
+              tma_load_3d_pair(sb, &map_z, bar, f0, tok, b);
+              tma_load_3d_pair(sb + state2::BKT * 128, &map_z, bar, f0 + 64, tok, b);
+            }
             ++p_issued;
             if (++p_stage == STAGES) {
               p_stage = 0;

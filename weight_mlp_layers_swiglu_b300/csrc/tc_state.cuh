@@ -50,6 +50,7 @@ struct Params {
   const float* W_init;          // optional [B, d, f] fp32: each sequence's own starting state
   int reverse;                  // 1: chunks run last to first (the backward pass's suffix scan)
   int no_snap;                  // 1: no W_eff snapshot at all, only the final state (update totals)
+  int blocked;                  // 1 (CTA-pair kernels): V and Z maps are 4-D, [B][n/64][T][64] blocks
   DevStatus st;
 };
 
