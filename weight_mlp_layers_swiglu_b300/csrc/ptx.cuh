@@ -327,6 +327,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
+// The same arrival without release semantics, for an epilogue warp that hands an accumulator
+// back to the MMA issuer after reading it: its tcgen05.ld have completed (tcgen05.wait::ld) and
+// been ordered by tcgen05.fence::before_thread_sync, and the waiter reads nothing the warp wrote
+// to memory.  The release form waits until all of the thread's earlier memory operations are
+// visible at cluster scope, which cost 3-4 thousand cycles per arrival in the state kernels.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // TMA tile loads into this CTA's shared memory whose byte count is signalled on an mbarrier of
 // either CTA of the pair (bar_cluster from cluster_addr).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int x,

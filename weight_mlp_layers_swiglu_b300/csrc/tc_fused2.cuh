@@ -370,10 +370,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lead_snap_done = cluster_addr(smem_u32(snap_done), 0);
     const uint32_t lead_acc_empty = cluster_addr(smem_u32(acc_empty), 0);
     const uint32_t lead_tile_empty = cluster_addr(smem_u32(tile_empty), 0);
-    auto release = [&](uint32_t lead_bar) {  // this warp is done with an accumulator
+    // this warp is done with an accumulator: after initialising it (tcgen05.st, release
+    // semantics) or after reading it (relaxed: the reads have completed)
+    auto release = [&](uint32_t lead_bar, bool after_reads = true) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(lead_bar);
+      if (lane == 0) {
+        if (after_reads)
+          mbar_arrive_cluster_relaxed(lead_bar);
+        else
+          mbar_arrive_cluster(lead_bar);
+      }
     };
     bool ok = true;
     int pending = -1;  // slice whose stores this warp issued last and has not published yet
@@ -406,7 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (pending >= 0) publish(pending);
           pending = slice;
         }
-        release(lead_snap_done + 8u * slot);
+        release(lead_snap_done + 8u * slot, false);
       }
       for (int i = 1; i <= S.n_chunks && ok; ++i) {
         for (int slot = 0; slot < 2; ++slot) {

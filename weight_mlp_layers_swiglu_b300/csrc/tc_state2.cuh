@@ -190,10 +190,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     OutStager out{out_stage + (warp - 2) * 2 * OUT_BOX_BYTES, 0u, lane};
     tma_prefetch_desc(&map_weff);
     tma_prefetch_desc(&map_wfin);
-    auto release = [&](int slot) {  // this warp is done with the unit's accumulator
+    // this warp is done with the unit's accumulator: after initialising it (tcgen05.st, release
+    // semantics) or after reading it (relaxed: the reads have completed)
+    auto release = [&](int slot, bool after_reads) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&snap_done[slot]), 0));
+      if (lane == 0) {
+        const uint32_t bar = cluster_addr(smem_u32(&snap_done[slot]), 0);
+        if (after_reads)
+          mbar_arrive_cluster_relaxed(bar);
+        else
+          mbar_arrive_cluster(bar);
+      }
     };
     uint32_t chunk_waits[2] = {0, 0};
     bool ok = true;
@@ -214,7 +222,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         tmem_st_wait();
         if (!p.skip_first && !p.no_snap)
           state::snapshot_bf16(out, t_row, &map_weff, nb * BNF, row0 + q * 32, b * p.n_chunks + state::chunk_at(p, 0));
-        release(slot);
+        release(slot, false);
       }
       for (int i = 1; i <= p.n_chunks && ok; ++i) {
         for (int slot = 0; slot < 2; ++slot) {
@@ -234,7 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             if (!p.no_snap)
               state::snapshot_bf16(out, t_row, &map_weff, nb * BNF, row0 + q * 32,
                                    b * p.n_chunks + state::chunk_at(p, i));
-            release(slot);
+            release(slot, true);
           } else {
             state::snapshot_f32(out, t_row, &map_wfin, nb * BNF, row0 + q * 32, b);
             tc_fence_before();
