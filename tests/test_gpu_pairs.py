@@ -73,6 +73,7 @@ def test_apply_pairs_match_single(ctx, B, T, d, f, C):
     (3, 600, 1024, 4096, 256, 4),   # 192 pair units: more unit pairs than co-resident CTA pairs
     (4, 9472, 512, 256, 256, 4),    # 148 apply tiles of 256 x 512: the fused kernel's wide tiles
     (2, 9472, 640, 256, 256, 3),    # wide tiles whose second 256-column half lies past d
+    (2, 700, 200, 328, 256, 4),     # widths that are not multiples of 64: V and Z through 3-D maps
 ])
 def test_layer_pairs_match_single(ctx, fused, B, T, d, f, C, k):
     w, x = random_case(B, T, d, f, C, k, 2.0 / C, "bf16", 60 + T)

@@ -55,6 +55,32 @@ struct Row8<float> {
   }
 };
 
+// The K taps of channels c0 .. c0+N-1, widened: w[e][s] = conv_w[c0 + e, s].  Those N*K values
+// are contiguous; with conv_w 16-byte aligned (c0 a multiple of 8 keeps the offset aligned) they
+// are read as N*K*sizeof(T)/16 vectors instead of N*K scalars, which had bounded the conv
+// kernel's rate (one scalar load per tap and channel against 11 row vectors of data).
+template <typename T, int K, int N>
+__device__ __forceinline__ void load_taps(const T* __restrict__ conv_w, int c0, float (&w)[N][K]) {
+  static_assert((N * K * (int)sizeof(T)) % 16 == 0, "taps in whole vectors");
+  const T* src = conv_w + (int64_t)c0 * K;
+  if ((reinterpret_cast<uintptr_t>(conv_w) & 15u) == 0) {
+    constexpr int NV = N * K * (int)sizeof(T) / 16;
+    uint4 v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = reinterpret_cast<const uint4*>(src)[i];
+    const T* t = reinterpret_cast<const T*>(v);
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+#pragma unroll
+      for (int s = 0; s < K; ++s) w[e][s] = static_cast<float>(t[e * K + s]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+#pragma unroll
+      for (int s = 0; s < K; ++s) w[e][s] = static_cast<float>(src[e * K + s]);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
   Row8<T> r;
@@ -106,10 +132,7 @@ __global__ void __launch_bounds__(32 * CONV_STRIPS, 4)
       raw[j].zero();
   }
   float w[8][K];
-#pragma unroll
-  for (int e = 0; e < 8; ++e)
-#pragma unroll
-    for (int s = 0; s < K; ++s) w[e][s] = static_cast<float>(conv_w[(int64_t)(c0 + e) * K + s]);
+  load_taps<T, K, 8>(conv_w, c0, w);
   float win[K][8];  // the last K input rows, widened
 #pragma unroll
   for (int j = 0; j < K - 1; ++j) raw[j].widen(win[j]);
