@@ -82,10 +82,11 @@ const char* ipttt_version(void);
 const char* ipttt_status_string(ipttt_status s);
 
 /* Create a context on CUDA device `device`, bound to `cuda_stream` (a cudaStream_t; NULL =
- * the legacy default stream).  Allocates a 8-byte device status word, CUDA events and two
- * internal streams (the upload and download streams of ipttt_layer_forward_host), each
- * ordered after and joined back into the context's stream by events; this is the only call
- * that allocates device memory.  *out receives the context.
+ * the legacy default stream).  Allocates a 8-byte device status word, CUDA events and three
+ * internal streams (the upload and download streams of ipttt_layer_forward_host, and the
+ * stream of the bf16 backward pass's target branch), each ordered after and joined back into
+ * the context's stream by events; this is the only call that allocates device memory.  *out
+ * receives the context.
  * Errors: INVALID_ARG (out == NULL, bad device), CUDA. */
 ipttt_status ipttt_create(ipttt_ctx** out, int device, void* cuda_stream);
 

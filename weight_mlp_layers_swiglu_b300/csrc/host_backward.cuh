@@ -338,15 +338,78 @@ ipttt_status run_backward_core(ipttt_ctx* ctx, const void* H, const void* X0, co
   const bool bf16 = dt == IPTTT_BF16;
   const int64_t df = d * f;
   if (bf16 && (s = ensure_attrs(ctx)) != IPTTT_OK) return s;
+  // The target branch needs only R (the reverse scan): dV = eta Z R^T (per chunk),
+  // dY = dV W_target^T, dW_target = Y^T dV (without a projection dY is dV itself), and the
+  // causal conv's adjoints.
+  auto target_branch = [&]() -> ipttt_status {
+    ipttt_status r;
+    if ((r = run_apply(ctx, Z, Rst, B, T, d, f, C, dt, dV, nullptr, eta)) != IPTTT_OK) return r;
+    if (Wt == nullptr) {
+      dY = dV;
+    } else if (bf16) {
+      if ((r = run_apply(ctx, dV, Wt, 1, BT, d, d, CT, dt, dY)) != IPTTT_OK) return r;
+      if ((r = launch_state_general(ctx, Y, d, dV, d, 1, BT, d, d, CT, nullptr, nullptr, true, false, nullptr, dWt)) !=
+          IPTTT_OK)
+        return r;
+    } else {
+      if ((r = sgemm(ctx, static_cast<const float*>(dV), d, 1, static_cast<const float*>(Wt), 1, d,
+                     static_cast<float*>(dY), d, BT, d, d, 1.f, 0.f)) != IPTTT_OK ||
+          (r = sgemm(ctx, static_cast<const float*>(Y), 1, d, static_cast<const float*>(dV), d, 1, dWt, d, d, d, BT, 1.f,
+                     0.f)) != IPTTT_OK)
+        return r;
+    }
+    const int64_t groups = d / (bf16 ? 8 : 4);  // 16-byte channel groups
+    dim3 gx(ceil_div(groups, 64), ceil_div(T, simt::CONVX_ROWS), (unsigned)B);
+    dim3 gw((unsigned)L.strips, ceil_div(groups, 64));
+    if (bf16)
+      launch_conv_adjoints<__nv_bfloat16>(ctx, gx, gw, dY, cw, X0, dX0, part, (int)T, (int)d, k);
+    else
+      launch_conv_adjoints<float>(ctx, gx, gw, dY, cw, X0, dX0, part, (int)T, (int)d, k);
+    simt::sum_strips_kernel<<<ceil_div(d * k, 256), 256, 0, ctx->stream>>>(part, dcw, (int)L.strips, d * k);
+    return check_launch(ctx, "conv backward launch");
+  };
   if (bf16) {
     // reverse scan: R_i = dW_final + sum_{l>i} dO_l^T Z_l, final = dW_final + sum_i dO_i^T Z_i
     if ((s = launch_state_general(ctx, dO, d, Z, f, B, T, d, f, C, nullptr, dW_final, false, true, Rst,
                                   B == 1 ? dW0 : dW0b)) != IPTTT_OK)
       return s;
+    // After the scan the target branch can run on the context's side stream, beside dZ, dH,
+    // dW_gate and dW_up on the caller's stream, so that the persistent kernels of one branch
+    // fill the SMs the other leaves idle.  That pays when the weight-gradient reductions have
+    // fewer 256 x 256 units than the grid has CTAs (at d = 1024, d_ff = 4096: 64 units, 12 %
+    // faster); with a full round of units or more (the 4B widths: 380) the two branches only
+    // contend, and it ran 1-4 % slower, so the branches then run in turn.  The branches read
+    // only what was written before the fork (the dZ step rewrites [A | U], which the target
+    // branch does not read) and write disjoint buffers; the caller's stream waits for the side
+    // stream at the end.
+    const bool fork = ceil_div(f, state2::BNF) * ceil_div(d, state2::PAIR_D) < (int64_t)ctx->pair_ctas;
+    cudaStream_t main = ctx->stream;
+    cudaError_t e;
+    if (fork && ((e = cudaEventRecord(ctx->b_fork, main)) != cudaSuccess ||
+                 (e = cudaStreamWaitEvent(ctx->side, ctx->b_fork, 0)) != cudaSuccess))
+      return cuda_fail(ctx, e, "backward fork");
+    if (fork) ctx->stream = ctx->side;
+    const ipttt_status sb = target_branch();
+    ctx->stream = main;
+    const size_t es = 2;
     // dZ_i = dO_i W_i + V_i R_i (V carries eta), and in the same epilogue the gated-MLP
     // adjoints: AU = [A | U] becomes [dA | dU]
-    if ((s = launch_two_seg(ctx, dO, d, V, d, 0, Wst, Rst, B * n, true, B, T, C, d, d, f, nullptr, AU)) != IPTTT_OK)
-      return s;
+    if (sb == IPTTT_OK &&
+        (s = launch_two_seg(ctx, dO, d, V, d, 0, Wst, Rst, B * n, true, B, T, C, d, d, f, nullptr, AU)) == IPTTT_OK &&
+        // dH = dA W_gate + dU W_up
+        (s = launch_two_seg(ctx, AU, 2 * f, nullptr, 2 * f, f, Wg, Wu, 1, false, 1, BT, CT, f, f, d, dH)) ==
+            IPTTT_OK &&
+        // dW_gate = dA^T H, dW_up = dU^T H (reductions over all tokens)
+        (s = launch_state_general(ctx, AU, 2 * f, H, d, 1, BT, f, d, CT, nullptr, nullptr, true, false, nullptr,
+                                  dWg)) == IPTTT_OK)
+      s = launch_state_general(ctx, static_cast<uint8_t*>(AU) + f * es, 2 * f, H, d, 1, BT, f, d, CT, nullptr,
+                               nullptr, true, false, nullptr, dWu);
+    // join even after an error, so that no work of this call is left unordered on the side stream
+    if (fork && ((e = cudaEventRecord(ctx->b_join, ctx->side)) != cudaSuccess ||
+                 (e = cudaStreamWaitEvent(main, ctx->b_join, 0)) != cudaSuccess))
+      return cuda_fail(ctx, e, "backward join");
+    if (sb != IPTTT_OK) return sb;
+    if (s != IPTTT_OK) return s;
   } else {
     float* rst = static_cast<float*>(Rst);
     // G_i = dO_i^T Z_i per chunk, then the reverse exclusive scan
@@ -363,25 +426,10 @@ ipttt_status run_backward_core(ipttt_ctx* ctx, const void* H, const void* X0, co
         (s = sgemm(ctx, static_cast<const float*>(V), d, 1, rst, f, 1, static_cast<float*>(dZ), f, C, f, d, 1.f, 1.f,
                    1, T, C, n, B, d, 0, f, 0, df, 0)) != IPTTT_OK)
       return s;
-  }
-  // fp32: the gated-MLP backward in place, AU -> [dA | dU] (bf16 did it in the dZ epilogue)
-  if (!bf16) {
+    // the gated-MLP backward in place, AU -> [dA | dU] (bf16 does it in the dZ epilogue)
     simt::swiglu_backward_kernel<float><<<ceil_div(BT * f, 256), 256, 0, ctx->stream>>>(
         static_cast<const float*>(dZ), static_cast<float*>(AU), BT, (int)f);
     if ((s = check_launch(ctx, "swiglu backward launch")) != IPTTT_OK) return s;
-  }
-  if (bf16) {
-    const size_t es = 2;
-    // dH = dA W_gate + dU W_up
-    if ((s = launch_two_seg(ctx, AU, 2 * f, nullptr, 2 * f, f, Wg, Wu, 1, false, 1, BT, CT, f, f, d, dH)) != IPTTT_OK)
-      return s;
-    // dW_gate = dA^T H, dW_up = dU^T H (reductions over all tokens)
-    if ((s = launch_state_general(ctx, AU, 2 * f, H, d, 1, BT, f, d, CT, nullptr, nullptr, true, false, nullptr,
-                                  dWg)) != IPTTT_OK ||
-        (s = launch_state_general(ctx, static_cast<uint8_t*>(AU) + f * es, 2 * f, H, d, 1, BT, f, d, CT, nullptr,
-                                  nullptr, true, false, nullptr, dWu)) != IPTTT_OK)
-      return s;
-  } else {
     const float* au = static_cast<const float*>(AU);
     if ((s = sgemm(ctx, au, 2 * f, 1, static_cast<const float*>(Wg), d, 1, static_cast<float*>(dH), d, BT, d, f, 1.f,
                    0.f)) != IPTTT_OK ||
@@ -390,35 +438,7 @@ ipttt_status run_backward_core(ipttt_ctx* ctx, const void* H, const void* X0, co
         (s = sgemm(ctx, au, 1, 2 * f, static_cast<const float*>(H), d, 1, dWg, d, f, d, BT, 1.f, 0.f)) != IPTTT_OK ||
         (s = sgemm(ctx, au + f, 1, 2 * f, static_cast<const float*>(H), d, 1, dWu, d, f, d, BT, 1.f, 0.f)) != IPTTT_OK)
       return s;
-  }
-  // dV = eta Z R^T (per chunk), dY = dV W_target^T, dW_target = Y^T dV (without a projection
-  // dY is dV itself)
-  if ((s = run_apply(ctx, Z, Rst, B, T, d, f, C, dt, dV, nullptr, eta)) != IPTTT_OK) return s;
-  if (Wt == nullptr) {
-    dY = dV;
-  } else if (bf16) {
-    if ((s = run_apply(ctx, dV, Wt, 1, BT, d, d, CT, dt, dY)) != IPTTT_OK) return s;
-    if ((s = launch_state_general(ctx, Y, d, dV, d, 1, BT, d, d, CT, nullptr, nullptr, true, false, nullptr, dWt)) !=
-        IPTTT_OK)
-      return s;
-  } else {
-    if ((s = sgemm(ctx, static_cast<const float*>(dV), d, 1, static_cast<const float*>(Wt), 1, d,
-                   static_cast<float*>(dY), d, BT, d, d, 1.f, 0.f)) != IPTTT_OK ||
-        (s = sgemm(ctx, static_cast<const float*>(Y), 1, d, static_cast<const float*>(dV), d, 1, dWt, d, d, d, BT, 1.f,
-                   0.f)) != IPTTT_OK)
-      return s;
-  }
-  // the causal conv's adjoints
-  {
-    const int64_t groups = d / (bf16 ? 8 : 4);  // 16-byte channel groups
-    dim3 gx(ceil_div(groups, 64), ceil_div(T, simt::CONVX_ROWS), (unsigned)B);
-    dim3 gw((unsigned)L.strips, ceil_div(groups, 64));
-    if (bf16)
-      launch_conv_adjoints<__nv_bfloat16>(ctx, gx, gw, dY, cw, X0, dX0, part, (int)T, (int)d, k);
-    else
-      launch_conv_adjoints<float>(ctx, gx, gw, dY, cw, X0, dX0, part, (int)T, (int)d, k);
-    simt::sum_strips_kernel<<<ceil_div(d * k, 256), 256, 0, ctx->stream>>>(part, dcw, (int)L.strips, d * k);
-    if ((s = check_launch(ctx, "conv backward launch")) != IPTTT_OK) return s;
+    if ((s = target_branch()) != IPTTT_OK) return s;
   }
   // the shared initial fast weight: sum over sequences (one sequence wrote it directly)
   if (B > 1) simt::sum_strips_kernel<<<ceil_div(df, 256), 256, 0, ctx->stream>>>(dW0b, dW0, (int)B, df);

@@ -71,6 +71,10 @@ struct ipttt_ctx {
   // copy_out overlap the compute on `stream` (per-piece events in piece_ev).
   cudaStream_t copy_in = nullptr, copy_out = nullptr;
   cudaEvent_t h_fork = nullptr, h_join = nullptr;
+  // The bf16 backward pass runs its target branch (dV, dY, dW_target, the conv adjoints) on
+  // `side`, forked from and joined back into `stream` with b_fork / b_join.
+  cudaStream_t side = nullptr;
+  cudaEvent_t b_fork = nullptr, b_join = nullptr;
   std::vector<cudaEvent_t> piece_ev;  // [2 * kMaxPieces]: upload done, compute done
   // timing
   bool timing = false;

@@ -65,7 +65,10 @@ ipttt_status ipttt_create(ipttt_ctx** out, int device, void* stream) {
   if (cudaStreamCreateWithFlags(&ctx->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&ctx->copy_out, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&ctx->h_fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ctx->h_join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventCreateWithFlags(&ctx->h_join, cudaEventDisableTiming) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->b_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->b_join, cudaEventDisableTiming) != cudaSuccess) {
     ipttt_destroy(ctx);
     return IPTTT_ERR_CUDA;
   }
@@ -164,6 +167,9 @@ void ipttt_destroy(ipttt_ctx* ctx) {
     if (e) cudaEventDestroy(e);
   if (ctx->h_fork) cudaEventDestroy(ctx->h_fork);
   if (ctx->h_join) cudaEventDestroy(ctx->h_join);
+  if (ctx->b_fork) cudaEventDestroy(ctx->b_fork);
+  if (ctx->b_join) cudaEventDestroy(ctx->b_join);
+  if (ctx->side) cudaStreamDestroy(ctx->side);
   if (ctx->copy_in) cudaStreamDestroy(ctx->copy_in);
   if (ctx->copy_out) cudaStreamDestroy(ctx->copy_out);
   if (ctx->status) cudaFree(ctx->status);
