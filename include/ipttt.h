@@ -239,7 +239,8 @@ ipttt_status ipttt_host_workspace_size(int64_t B, int64_t T, int64_t d, int64_t 
 /* The whole layer with the activations and results in HOST memory (pinned memory gives
  * asynchronous copies): H_host, X0_host [B,T,d] dtype in, O_host [B,T,d] dtype and
  * W_final_host [B,d,d_ff] fp32 out; the frozen weights stay device pointers.  The call runs in
- * pieces of about 4096 tokens (a multiple of C, at most 64 pieces): piece j is uploaded on an
+ * pieces of about 4096 tokens (a multiple of C, at most 64 pieces; with several pieces the
+ * last one's tokens are cut into halves of halves down to C): piece j is uploaded on an
  * internal copy stream, computed on the context's stream as a resumed call (the state and conv
  * halo of piece j-1), and its O downloaded on a second copy stream, so the copies of one piece
  * overlap the compute of its neighbours.  Pieces start at multiples of C, so the results equal

@@ -680,10 +680,30 @@ ipttt_status ipttt_layer_forward_host(ipttt_ctx* ctx, const void* H_host, const 
                      nullptr, Wst, ws)) != IPTTT_OK)
     return s;
   const size_t row_bytes = (size_t)T * d * es;  // one sequence in the host arrays
-  const int n_pieces = (int)((T + P - 1) / P);
-  for (int j = 0; j < n_pieces; ++j) {
-    const int64_t lo = j * P;
-    const int64_t len = (lo + P < T ? P : T - lo);
+  // Pieces of P tokens, except that when there are several, the last P tokens (or what remains)
+  // go in halves of halves down to C: after the last upload only a short piece computes and
+  // downloads before the final state does.  Every piece but the last is a multiple of C.
+  int64_t lens[kMaxPieces];
+  int n_pieces = 0;
+  {
+    int64_t rem = T;
+    while (rem > P) {
+      lens[n_pieces++] = P;
+      rem -= P;
+    }
+    if (n_pieces > 0) {
+      while (rem > C && n_pieces + 1 < kMaxPieces) {
+        const int64_t h = (rem / 2 + C - 1) / C * C;  // a multiple of C, at least half
+        if (h >= rem) break;
+        lens[n_pieces++] = h;
+        rem -= h;
+      }
+    }
+    lens[n_pieces++] = rem;
+  }
+  int64_t lo = 0;
+  for (int j = 0; j < n_pieces; lo += lens[j], ++j) {
+    const int64_t len = lens[j];
     const size_t off = (size_t)B * lo * d * es;   // piece j's [B, len, d] block of the staging
     const size_t width = (size_t)len * d * es;
     cudaEvent_t in_done = ctx->piece_ev[2 * j], comp_done = ctx->piece_ev[2 * j + 1];
