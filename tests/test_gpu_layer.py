@@ -105,8 +105,8 @@ def test_deterministic(ctx):
 @pytest.mark.parametrize("dt,B,T,d,f,C,k", [
     ("bf16", 2, 384, 256, 512, 128, 4),     # one piece
     ("bf16", 2, 9000, 256, 512, 1024, 4),   # three pieces (4096, 4096, 808): uploads, compute and downloads overlap
-    ("bf16", 1, 12288, 128, 256, 512, 1),   # three whole pieces, no conv halo
-    ("f32", 2, 5000, 64, 128, 48, 3),       # pieces of 4128 tokens
+    ("bf16", 1, 12288, 128, 256, 512, 1),   # 4096, 4096, then the last 4096 as 2048, 1024, 512, 512; no conv halo
+    ("f32", 2, 5000, 64, 128, 48, 3),       # 4128, then 480, 240, 96, 48 and a ragged 8
 ])
 def test_host_buffer_entry_point_matches(ctx, dt, B, T, d, f, C, k):
     """The host-buffer entry runs a call in pieces (multiples of C) whose copies overlap the
