@@ -308,14 +308,15 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
                            gemm::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "smem attribute (two-segment)");
   {
-    constexpr int NPK = 15;
+    constexpr int NPK = 16;
     const void* pk[NPK] = {(const void*)gemm2::tc_gemm2_kernel<gemm::kSwiglu>,
                            (const void*)gemm2::tc_gemm2_kernel<gemm::kTarget>,
                            (const void*)gemm2::tc_gemm2_kernel<gemm::kApply>,
                            (const void*)gemm2::tc_gemm2_kernel<gemm::kSwigluSave>,
                            (const void*)gemm2::tc_gemm2_kernel<gemm::kTwoSeg>,
                            (const void*)state2::tc_state2_kernel,
-                           (const void*)fused2::tc_state_apply2_kernel,
+                           (const void*)fused2::tc_state_apply2_kernel<1>,
+                           (const void*)fused2::tc_state_apply2_kernel<2>,
                            (const void*)tconv2::tc_target_conv2_kernel<1>,
                            (const void*)tconv2::tc_target_conv2_kernel<2>,
                            (const void*)tconv2::tc_target_conv2_kernel<3>,
@@ -326,9 +327,11 @@ ipttt_status ensure_attrs(ipttt_ctx* ctx) {
                            (const void*)tconv2::tc_target_conv2_kernel<8>};
     int pk_smem[NPK], pk_threads[NPK];
     for (int ki = 0; ki < NPK; ++ki) {
-      pk_smem[ki] = ki < 5 ? gemm2::SMEM_BYTES : ki == 5 ? state2::SMEM_BYTES : ki == 6 ? fused2::SMEM_BYTES
-                                                                                          : tconv2::SMEM_BYTES;
-      pk_threads[ki] = ki < 7 ? gemm2::NUM_THREADS : tconv2::NUM_THREADS;
+      pk_smem[ki] = ki < 5    ? gemm2::SMEM_BYTES
+                    : ki == 5 ? state2::SMEM_BYTES
+                    : ki < 8  ? fused2::SMEM_BYTES
+                              : tconv2::SMEM_BYTES;
+      pk_threads[ki] = ki < 8 ? gemm2::NUM_THREADS : tconv2::NUM_THREADS;
     }
     int clusters = 1 << 30;
     for (int ki = 0; ki < NPK; ++ki) {

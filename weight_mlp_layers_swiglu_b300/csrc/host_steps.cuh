@@ -378,7 +378,9 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, fused2::tc_state_apply2_kernel, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
+      p.a_halves == 2
+          ? cudaLaunchKernelEx(&cfg, fused2::tc_state_apply2_kernel<2>, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p)
+          : cudaLaunchKernelEx(&cfg, fused2::tc_state_apply2_kernel<1>, mv, mz, mw_st, mf, mza, mw_ld, mw0, mo, p);
   if (e != cudaSuccess) {
     cudaGetLastError();  // a refused launch configuration is not sticky
     // "too large": this context now has fewer SMs than the grid was sized for (the next call

@@ -42,7 +42,8 @@ struct Params {
   uint32_t* next_tile;    // apply-tile queue head
   uint32_t ready_target;  // m_units * n_units * 4
   int a_halves;           // CTA-pair kernel: 256-column halves per apply tile (2: 512 columns, one
-                          // accumulator; 1: 256 columns, two accumulators in turn)
+                          // accumulator; 1: 256 columns, two accumulators in turn); the host
+                          // launches the kernel instantiation of that width
 };
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {

@@ -61,6 +61,9 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// HALVES (= Params::a_halves): 256-column halves per apply tile, a template parameter so that
+// each tile width compiles to its own fixed loops.
+template <int HALVES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tc_state_apply2_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_z,
                            const __grid_constant__ CUtensorMap map_weff_st,
@@ -95,7 +98,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int n_cl = gridDim.x >> 1;
   const int upairs = (S.units + 1) / 2;
   const int total_tiles = A.problems * A.m_tiles * A.n_tiles;
-  const int halves = p.a_halves;                 // 1 or 2
+  constexpr int halves = HALVES;                 // 1 or 2
   const int tile_n = halves * gemm2::BN;         // O columns per apply tile
 
   if (threadIdx.x == 0) {
