@@ -101,6 +101,14 @@ ipttt_status ipttt_set_stream(ipttt_ctx* ctx, void* cuda_stream);
  * context, use two. */
 ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable);
 
+/* Width of the apply tiles of that cooperative kernel on CTA pairs: halves = 0 (default)
+ * chooses per call (256 x 512 tiles when d_ff / 64 >= 128 and they make at least two waves
+ * over the co-resident pairs, else 256 x 256), 1 always 256 x 256 (two accumulators in turn),
+ * 2 always 256 x 512 (one accumulator, a quarter fewer operand bytes per FLOP).  Results are
+ * bit-identical: every output element is the same fp32 sum in the same order.
+ * Errors: INVALID_ARG (halves not 0, 1 or 2). */
+ipttt_status ipttt_set_apply_tiles(ipttt_ctx* ctx, int halves);
+
 /* Choose how step (2) of a bf16 layer call runs: enable = 0 (default) as the conv kernel
  * (memory bound, before step (1)) followed by the W_target GEMM; enable = 1 as one kernel on
  * CTA pairs whose extra warps form each tile of the conv output Y = CausalConv1D(X0) in

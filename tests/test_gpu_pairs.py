@@ -66,24 +66,28 @@ def test_apply_pairs_match_single(ctx, B, T, d, f, C):
         assert rel_err(a[bb], oracle.chunk_apply(Z[bb].cpu(), W[bb].cpu(), C)) <= 1e-2
 
 
-@pytest.mark.parametrize("fused", [True, False])
+# tail: "unfused" = the state and apply kernels; the fused kernel with its apply tiles chosen per
+# call ("auto"), 256 x 256 ("narrow") or 256 x 512 ("wide")
+@pytest.mark.parametrize("tail", ["unfused", "auto", "narrow", "wide"])
 @pytest.mark.parametrize("B,T,d,f,C,k", [
     (2, 700, 256, 512, 256, 4),
     (1, 1100, 384, 768, 512, 3),
     (3, 600, 1024, 4096, 256, 4),   # 192 pair units: more unit pairs than co-resident CTA pairs
-    (4, 9472, 512, 256, 256, 4),    # 148 apply tiles of 256 x 512: the fused kernel's wide tiles
+    (4, 9472, 512, 256, 256, 4),    # 148 apply tiles of 256 x 512, two waves of wide tiles
     (2, 9472, 640, 256, 256, 3),    # wide tiles whose second 256-column half lies past d
     (2, 700, 200, 328, 256, 4),     # widths that are not multiples of 64: V and Z through 3-D maps
 ])
-def test_layer_pairs_match_single(ctx, fused, B, T, d, f, C, k):
+def test_layer_pairs_match_single(ctx, tail, B, T, d, f, C, k):
     w, x = random_case(B, T, d, f, C, k, 2.0 / C, "bf16", 60 + T)
     xd = to_dev(x)
-    ctx.set_fused_tail(fused)
+    ctx.set_fused_tail(tail != "unfused")
+    ctx.set_apply_tiles({"unfused": 0, "auto": 0, "narrow": 1, "wide": 2}[tail])
     try:
         (Oa, Wa), (Ob, Wb) = both(ctx, lambda: tuple(t.clone() for t in ctx.layer_forward(
             xd["H"], xd["X0"], xd["W_gate"], xd["W_up"], xd["W_down0"], xd["W_target"], xd["conv_w"], C, w.eta)))
     finally:
         ctx.set_fused_tail(True)
+        ctx.set_apply_tiles(0)
     assert torch.equal(Oa, Ob) and torch.equal(Wa, Wb)
     O_ref, W_ref = oracle.layer_forward(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_down0"], x["W_target"],
                                         x["conv_w"], C, w.eta)
@@ -134,3 +138,15 @@ def test_resume_pairs_match_single(ctx, B, T, d, f, C):
     O_ref, W_ref, _ = oracle.layer_resume(x["H"], x["X0"], x["W_gate"], x["W_up"], x["W_target"], x["conv_w"],
                                           W_state.cpu(), halo.cpu(), C, w.eta)
     assert rel_err(Oa, O_ref) <= TOL["bf16"] and rel_err(Wa, W_ref) <= TOL["bf16"]
+
+
+def test_apply_tile_width_argument(ctx):
+    """ipttt_set_apply_tiles takes 0 (per call), 1 or 2 and refuses anything else."""
+    import weight_mlp_layers_swiglu_b300 as pkg
+
+    for h in (1, 2, 0):
+        ctx.set_apply_tiles(h)
+    for bad in (-1, 3):
+        with pytest.raises(pkg.IptttError) as e:
+            ctx.set_apply_tiles(bad)
+        assert e.value.status == 1

@@ -65,6 +65,7 @@ struct ipttt_ctx {
   bool cta_pairs = true;   // bf16 GEMMs on CTA pairs (cta_group::2) when the device allows
   int pair_ctas = 0;       // CTAs of the pair GEMM grid (2 x co-resident clusters; 0 = unavailable)
   bool fused_pairs = true; // the cooperative launch of the fused pair kernel has not been refused
+  int apply_halves = 0;    // fused pair kernel's apply tiles: 0 per call, 1 = 256 x 256, 2 = 256 x 512
   bool fused_target = false;  // step (2) as one kernel (conv inside the target GEMM) when pairs run
   int target_shift = 0;    // 1: the conv window of the target ends at the next token
   // The host-buffer entry pipelines pieces of a call: uploads on copy_in and downloads on

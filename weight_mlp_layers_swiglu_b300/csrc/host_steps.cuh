@@ -351,10 +351,14 @@ bool launch_state_apply_pairs(ipttt_ctx* ctx, const void* V, const void* Z, cons
   p.s.W_init = W_init;
   p.s.blocked = blocked;
   p.s.st = dev_status(ctx);
-  // 256 x 512 apply tiles when they still make two waves over the co-resident pairs, else
-  // 256 x 256 tiles (twice as many) so that a short call keeps more pairs busy
+  // 256 x 512 apply tiles (a quarter fewer operand bytes per FLOP, one accumulator whose epilogue
+  // is not hidden) when a tile is long, d_ff / 64 >= 128 k-blocks, and the wide tiles still
+  // make two waves over the co-resident pairs; else 256 x 256 tiles, two accumulators in turn.
+  // Measured on one box with both instantiations: wide 0.5-1.2 % faster at d_ff = 9728 (152
+  // k-blocks), narrow 2-4.5 % faster at d_ff = 4096 (64 k-blocks).
   const int64_t wide_tiles = B * n * (C / gemm2::PAIR_M) * ceil_div(d, 2 * gemm2::BN);
-  p.a_halves = wide_tiles >= (int64_t)ctx->pair_ctas ? 2 : 1;
+  p.a_halves = ctx->apply_halves != 0 ? ctx->apply_halves
+               : (wide_tiles >= (int64_t)ctx->pair_ctas && ceil_div(f, gemm2::BK) >= 128) ? 2 : 1;
   p.a.m_tiles = (int)(C / gemm2::PAIR_M);
   p.a.n_tiles = ceil_div(d, p.a_halves * gemm2::BN);
   p.a.k_blocks = ceil_div(f, gemm2::BK);

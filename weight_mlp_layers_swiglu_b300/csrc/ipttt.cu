@@ -126,6 +126,16 @@ ipttt_status ipttt_set_fused_tail(ipttt_ctx* ctx, int enable) {
   return IPTTT_OK;
 }
 
+ipttt_status ipttt_set_apply_tiles(ipttt_ctx* ctx, int halves) {
+  if (!ctx) return IPTTT_ERR_INVALID_ARG;
+  if (halves < 0 || halves > 2) {
+    set_err(ctx, "apply tiles: halves = %d (0 = per call, 1 = 256 x 256, 2 = 256 x 512)", halves);
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  ctx->apply_halves = halves;
+  return IPTTT_OK;
+}
+
 ipttt_status ipttt_set_wait_limit_ns(ipttt_ctx* ctx, uint64_t ns) {
   if (!ctx) return IPTTT_ERR_INVALID_ARG;
   if (ns == 0) {

@@ -32,6 +32,7 @@ _SIGNATURES = {
     "ipttt_set_stream": (ctypes.c_int, [c_vp, c_vp]),
     "ipttt_set_wait_limit_ns": (ctypes.c_int, [c_vp, ctypes.c_uint64]),
     "ipttt_set_fused_tail": (ctypes.c_int, [c_vp, ctypes.c_int]),
+    "ipttt_set_apply_tiles": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_set_fused_target": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_set_cta_pairs": (ctypes.c_int, [c_vp, ctypes.c_int]),
     "ipttt_set_target_shift": (ctypes.c_int, [c_vp, ctypes.c_int]),
@@ -212,6 +213,10 @@ class Context:
 
     def set_fused_tail(self, enable: bool):
         self._check(self.lib.ipttt_set_fused_tail(self.h, 1 if enable else 0), "set_fused_tail")
+
+    def set_apply_tiles(self, halves: int):
+        """0: per call (default); 1: 256 x 256 apply tiles; 2: 256 x 512 (the fused pair kernel)."""
+        self._check(self.lib.ipttt_set_apply_tiles(self.h, int(halves)), "set_apply_tiles")
 
     def set_cta_pairs(self, enable: bool):
         self._check(self.lib.ipttt_set_cta_pairs(self.h, 1 if enable else 0), "set_cta_pairs")
